@@ -1,0 +1,136 @@
+"""CPU oracle for the batch-invariant W8A8 verify-pass linear (test infrastructure).
+
+Only the tests, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline leg
+may import this package.  The library under test never imports it, and it
+imports nothing from the library.  Every function is a thin numpy/ctypes
+wrapper over the plain C in ``oracle.c``, where each step cites the page it
+follows.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import numpy as np
+
+from . import build as _build
+
+_LIB = None
+
+
+def lib():
+    global _LIB
+    if _LIB is None:
+        L = ctypes.CDLL(_build.build())
+        vp, i64, ci = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        L.oracle_bf16_to_f32.argtypes = [ctypes.c_uint16]
+        L.oracle_bf16_to_f32.restype = ctypes.c_float
+        L.oracle_f32_to_bf16_rne.argtypes = [ctypes.c_float]
+        L.oracle_f32_to_bf16_rne.restype = ctypes.c_uint16
+        L.oracle_f32_to_bf16_rne_array.argtypes = [vp, i64, vp]
+        L.oracle_f32_to_bf16_rne_array.restype = None
+        L.oracle_quantize_act.argtypes = [vp, i64, ci, ci, vp, vp]
+        L.oracle_quantize_act.restype = None
+        L.oracle_quantize_weight.argtypes = [vp, ci, ci, vp, vp]
+        L.oracle_quantize_weight.restype = None
+        L.oracle_requant_pow2.argtypes = [vp, vp, ci, ci, vp, vp]
+        L.oracle_requant_pow2.restype = None
+        L.oracle_linear_w8a8.argtypes = [vp, vp, ci, ci, vp, vp, ci, vp]
+        L.oracle_linear_w8a8.restype = ci
+        L.oracle_lmhead_argmax.argtypes = [vp, vp, ci, ci, vp, vp, ci, vp, vp]
+        L.oracle_lmhead_argmax.restype = ci
+        L.oracle_num_threads.argtypes = []
+        L.oracle_num_threads.restype = ci
+        _LIB = L
+    return _LIB
+
+
+def _c(a: np.ndarray, dtype) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    assert a.dtype == dtype, (a.dtype, dtype)
+    return a
+
+
+def bf16_to_f32(b: int) -> float:
+    return float(lib().oracle_bf16_to_f32(int(b)))
+
+
+def f32_to_bf16_rne(f: float) -> int:
+    return int(lib().oracle_f32_to_bf16_rne(float(np.float32(f))))
+
+
+def f32_to_bf16_rne_array(f: np.ndarray) -> np.ndarray:
+    f = _c(f, np.float32)
+    out = np.empty(f.shape, np.uint16)
+    lib().oracle_f32_to_bf16_rne_array(f.ctypes.data, f.size, out.ctypes.data)
+    return out
+
+
+def quantize_act(x_bf16: np.ndarray, K: int | None = None):
+    """x_bf16: uint16 [M, ldx] bf16 patterns; the first K columns are the row.
+    Returns (q int8 [M, K], s_a float32 [M])."""
+    x = _c(x_bf16, np.uint16)
+    M, ldx = x.shape
+    K = ldx if K is None else K
+    q = np.empty((M, K), np.int8)
+    s = np.empty(M, np.float32)
+    lib().oracle_quantize_act(x.ctypes.data, ldx, M, K, q.ctypes.data, s.ctypes.data)
+    return q, s
+
+
+def quantize_weight(w_f32: np.ndarray):
+    """Checkpoint-style absmax quantisation: (W_q int8 [N, K], s_w float32 [N])."""
+    w = _c(w_f32, np.float32)
+    N, K = w.shape
+    q = np.empty((N, K), np.int8)
+    s = np.empty(N, np.float32)
+    lib().oracle_quantize_weight(w.ctypes.data, N, K, q.ctypes.data, s.ctypes.data)
+    return q, s
+
+
+def requant_pow2(wq: np.ndarray, s_w: np.ndarray):
+    wq = _c(wq, np.int8)
+    s_w = _c(s_w, np.float32)
+    N, K = wq.shape
+    out = np.empty_like(wq)
+    so = np.empty_like(s_w)
+    lib().oracle_requant_pow2(wq.ctypes.data, s_w.ctypes.data, N, K, out.ctypes.data, so.ctypes.data)
+    return out, so
+
+
+def linear_w8a8(q: np.ndarray, s_a: np.ndarray, wq: np.ndarray, s_w: np.ndarray) -> np.ndarray:
+    """bf16 patterns y [M, N]; raises OverflowError if the int32 bound is broken."""
+    q = _c(q, np.int8)
+    s_a = _c(s_a, np.float32)
+    wq = _c(wq, np.int8)
+    s_w = _c(s_w, np.float32)
+    M, K = q.shape
+    N, K2 = wq.shape
+    assert K == K2
+    y = np.empty((M, N), np.uint16)
+    rc = lib().oracle_linear_w8a8(q.ctypes.data, s_a.ctypes.data, M, K, wq.ctypes.data,
+                                  s_w.ctypes.data, N, y.ctypes.data)
+    if rc != 0:
+        raise OverflowError("an int8 dot product reached 2^31")
+    return y
+
+
+def lmhead_argmax(q, s_a, wq, s_w, want_logits: bool = True):
+    q = _c(q, np.int8)
+    s_a = _c(s_a, np.float32)
+    wq = _c(wq, np.int8)
+    s_w = _c(s_w, np.float32)
+    M, K = q.shape
+    N = wq.shape[0]
+    logits = np.empty((M, N), np.uint16) if want_logits else None
+    am = np.empty(M, np.int32)
+    rc = lib().oracle_lmhead_argmax(q.ctypes.data, s_a.ctypes.data, M, K, wq.ctypes.data,
+                                    s_w.ctypes.data, N,
+                                    logits.ctypes.data if logits is not None else None,
+                                    am.ctypes.data)
+    if rc != 0:
+        raise OverflowError("an int8 dot product reached 2^31")
+    return am, logits
+
+
+def num_threads() -> int:
+    return int(lib().oracle_num_threads())

@@ -1,0 +1,264 @@
+/*
+ * CPU oracle for the batch-invariant W8A8 verify-pass linear layer.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the
+ * benchmark's CPU-baseline leg may load this file's library.  It shares no
+ * code, header or table with the CUDA library and calls nothing in it.
+ *
+ * Plain scalar C, built with -O2 -ffp-contract=off and no fast-math, so every
+ * float operation below is one IEEE-754 operation rounded to nearest-even.
+ * Sums of int8 products are carried in int64 (exact) and checked against the
+ * int32 range.  Loops run in the textbook order; the only parallelism is an
+ * OpenMP loop over independent output elements, which cannot change a result.
+ *
+ * Sources (page title, section / table):
+ *  [chen]   "Deterministic LLM Inference Across GPU Kernels: Power-of-Two INT8
+ *           Quantization Scales and the Limits of Tolerance-Based Conformance",
+ *           Abstract, Fig. 1, Table II (epilogue faults F1-F5).
+ *  [alibi]  "The Integer Alibi: Localizing Cross-Kernel Divergence in
+ *           INT8-Quantized LLM Inference" (abstract on the same page).
+ *  [cintu]  "why speculative decoding changed my output", sections
+ *           "floats care about order" and "the mat-vec kernel".
+ *  [goyal]  "My speculative decoder got slower", sections "Why the decoders
+ *           disagreed?" (bf16 tie 30.0 / 29.875) and "We're nowhere near SOL"
+ *           (a vocab head that computes only the winning token).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------ bf16 */
+
+/* bf16 -> fp32 is exact: a bf16 value is the top half of an fp32 pattern. */
+float oracle_bf16_to_f32(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+/*
+ * fp32 -> bf16, round to nearest, ties to even (the output rounding the
+ * epilogue must use; output truncation is fault F4 in [chen] Table II).
+ * Written from the definition: the two bf16 neighbours of f are the pattern
+ * with the low 16 bits cleared (toward zero) and the next pattern away from
+ * zero; pick the one nearer to f, and the one with an even last bit on a tie.
+ * The distances are exact in double (f has 24 significant bits).  Overflow
+ * rounds to infinity exactly as IEEE round-to-nearest does; NaN becomes the
+ * quiet NaN 0x7FC0 (the oracle never produces one from finite inputs).
+ */
+uint16_t oracle_f32_to_bf16_rne(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    if (isnan(f))
+        return 0x7FC0;
+    uint16_t toward0 = (uint16_t)(u >> 16);
+    if ((u & 0xFFFFu) == 0)
+        return toward0;                      /* already a bf16 value */
+    uint16_t away = (uint16_t)(toward0 + 1); /* next magnitude (may be Inf) */
+    double vf = (double)f;
+    double v0 = (double)oracle_bf16_to_f32(toward0);
+    double v1;
+    if ((away & 0x7FFFu) == 0x7F80u) {
+        /* the next magnitude is infinity: compare with 2^128, the value the
+           unbounded-exponent format would hold there */
+        v1 = (away & 0x8000u) ? -ldexp(1.0, 128) : ldexp(1.0, 128);
+    } else {
+        v1 = (double)oracle_bf16_to_f32(away);
+    }
+    double d0 = fabs(vf - v0), d1 = fabs(v1 - vf);
+    if (d0 < d1) return toward0;
+    if (d1 < d0) return away;
+    return (toward0 & 1u) ? away : toward0;   /* tie: even last bit */
+}
+
+/* Array form of oracle_f32_to_bf16_rne, for exhaustive checks. */
+void oracle_f32_to_bf16_rne_array(const float *f, int64_t n, uint16_t *out)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = oracle_f32_to_bf16_rne(f[i]);
+}
+
+/* Round a double to the nearest integer, ties to even, written out. */
+static double rne_to_int(double v)
+{
+    double fl = floor(v);
+    double frac = v - fl;                   /* exact for |v| < 2^52 */
+    if (frac > 0.5) return fl + 1.0;
+    if (frac < 0.5) return fl;
+    return (fmod(fl, 2.0) == 0.0) ? fl : fl + 1.0;
+}
+
+static int8_t clamp127(double r)
+{
+    if (r > 127.0) r = 127.0;
+    if (r < -127.0) r = -127.0;
+    return (int8_t)r;
+}
+
+/* ------------------------------------------------ per-row absmax quantisation
+ *
+ * W8A8 (the "INT8 pipeline" of [chen] Abstract / Fig. 1; the scale rule is the
+ * plain absmax one): s = absmax / 127 as one IEEE fp32 division (s = 1 for an
+ * all-zero row), q = clamp(rne(v / s), -127, 127) with the quotient an IEEE
+ * fp32 division.  -128 is never produced.
+ */
+static void quantize_row_f32(const float *v, int K, int8_t *q, float *s_out)
+{
+    float amax = 0.0f;
+    for (int k = 0; k < K; ++k) {
+        float a = fabsf(v[k]);
+        if (a > amax) amax = a;
+    }
+    float s = (amax == 0.0f) ? 1.0f : amax / 127.0f;
+    for (int k = 0; k < K; ++k) {
+        float t = v[k] / s;                 /* fp32 division, RNE */
+        q[k] = clamp127(rne_to_int((double)t));
+    }
+    *s_out = s;
+}
+
+/* A1: per-token activation quantisation of bf16 x [M, K] (row stride ldx). */
+void oracle_quantize_act(const uint16_t *x, int64_t ldx, int M, int K, int8_t *q, float *s_a)
+{
+    float *row = (float *)malloc(sizeof(float) * (size_t)K);
+    for (int m = 0; m < M; ++m) {
+        for (int k = 0; k < K; ++k)
+            row[k] = oracle_bf16_to_f32(x[(int64_t)m * ldx + k]);
+        quantize_row_f32(row, K, q + (int64_t)m * K, &s_a[m]);
+    }
+    free(row);
+}
+
+/* Checkpoint-style per-output-channel weight quantisation of fp32 W [N, K]. */
+void oracle_quantize_weight(const float *w, int N, int K, int8_t *wq, float *s_w)
+{
+#pragma omp parallel for schedule(static)
+    for (int n = 0; n < N; ++n)
+        quantize_row_f32(w + (int64_t)n * K, K, wq + (int64_t)n * K, &s_w[n]);
+}
+
+/* --------------------------------------------- power-of-two requantisation
+ *
+ * [chen] Abstract and Fig. 1: every weight scale moves to its nearest power
+ * of two, and the weights are requantised to the new scale (rewriting the
+ * scale alone is the artefact the paper warns about).
+ *
+ * Reading: "nearest" is taken in the log domain, s' = 2^round(log2 s).  With
+ * s = m * 2^E, m in [0.5, 1) (frexp), log2 s = E + log2 m and log2 m is in
+ * [-1, 0), so s' = 2^E when m >= 2^-1/2, else 2^(E-1).  m >= 2^-1/2 is decided
+ * exactly as m*m >= 0.5 (m has 24 bits, m*m is exact in double).  A tie would
+ * need m = 2^-1/2, which is irrational, so none exists.  The new codes are
+ * clamp(rne(q * s / s'), -127, 127), each product exact in double.  A scale
+ * whose power of two would overflow fp32 is held at 2^127.  Rows whose scale
+ * is not a positive finite number are copied unchanged.
+ */
+void oracle_requant_pow2(const int8_t *wq, const float *s_w, int N, int K,
+                         int8_t *wq_out, float *s_out)
+{
+#pragma omp parallel for schedule(static)
+    for (int n = 0; n < N; ++n) {
+        float s = s_w[n];
+        const int8_t *src = wq + (int64_t)n * K;
+        int8_t *dst = wq_out + (int64_t)n * K;
+        if (!(s > 0.0f) || isinf(s)) {
+            memmove(dst, src, (size_t)K);
+            s_out[n] = s;
+            continue;
+        }
+        int E;
+        double m = frexp((double)s, &E);
+        int e2 = (m * m >= 0.5) ? E : E - 1;
+        if (e2 > 127) e2 = 127;
+        double sp = ldexp(1.0, e2);
+        for (int k = 0; k < K; ++k) {
+            double v = (double)src[k] * (double)s / sp;
+            dst[k] = clamp127(rne_to_int(v));
+        }
+        s_out[n] = (float)sp;
+    }
+}
+
+/* ------------------------------------------------------- linear + epilogue
+ *
+ * acc[m,n] = sum_k q[m,k] * W[n,k]   exact integer sum ([alibi]: for shared
+ *            int8 operands under a no-overflow bound the int32 dot product is
+ *            exact and independent of order; K * 127^2 < 2^31).
+ * y[m,n]   = bf16_rne( (float(acc) * s_a[m]) * s_w[n] )
+ *            [chen] Table II read as the correct epilogue: scales stay fp32
+ *            (not F1), the two multiplies are separate fp32 roundings with no
+ *            bf16 rounding between them (not F2), acc*s_a first, then *s_w
+ *            (not F3), one final round-to-nearest-even (not F4), scales never
+ *            enter the integer sum (not F5).  int32 -> fp32 rounds to nearest
+ *            even (C conversion in the default rounding mode).
+ * Returns 0, or -1 if some |acc| reached 2^31 (the overflow precondition).
+ */
+int oracle_linear_w8a8(const int8_t *q, const float *s_a, int M, int K,
+                       const int8_t *wq, const float *s_w, int N, uint16_t *y)
+{
+    int bad = 0;
+#pragma omp parallel for schedule(static) reduction(| : bad)
+    for (int n = 0; n < N; ++n) {
+        const int8_t *w = wq + (int64_t)n * K;
+        for (int m = 0; m < M; ++m) {
+            const int8_t *a = q + (int64_t)m * K;
+            int64_t acc = 0;
+            for (int k = 0; k < K; ++k)
+                acc += (int64_t)a[k] * (int64_t)w[k];
+            if (acc >= 2147483648LL || acc <= -2147483648LL) {
+                bad = 1;
+                acc = 0;
+            }
+            float f = (float)(int32_t)acc;
+            f = f * s_a[m];
+            f = f * s_w[n];
+            y[(int64_t)m * N + n] = oracle_f32_to_bf16_rne(f);
+        }
+    }
+    return bad ? -1 : 0;
+}
+
+/*
+ * Greedy LM-head argmax over the bf16 logits of each row: the lowest index n
+ * whose logit equals the row maximum, logits compared as real numbers (so -0
+ * equals +0).  Greedy decoding keeps the target's own argmax ([cintu] intro,
+ * [goyal] "Speculative decoding (SD)"); [goyal] shows bf16 logits tying
+ * (29.875 vs 29.875), so the tie rule is part of the contract.  The head
+ * reuses oracle_linear_w8a8 for the logits; `logits` may be NULL.
+ */
+int oracle_lmhead_argmax(const int8_t *q, const float *s_a, int M, int K,
+                         const int8_t *wq, const float *s_w, int N,
+                         uint16_t *logits, int32_t *argmax)
+{
+    uint16_t *y = logits ? logits : (uint16_t *)malloc(sizeof(uint16_t) * (size_t)M * (size_t)N);
+    int rc = oracle_linear_w8a8(q, s_a, M, K, wq, s_w, N, y);
+    for (int m = 0; m < M; ++m) {
+        int32_t best = 0;
+        float bv = oracle_bf16_to_f32(y[(int64_t)m * N]);
+        for (int n = 1; n < N; ++n) {
+            float v = oracle_bf16_to_f32(y[(int64_t)m * N + n]);
+            if (v > bv) {
+                bv = v;
+                best = n;
+            }
+        }
+        argmax[m] = best;
+    }
+    if (!logits) free(y);
+    return rc;
+}
+
+/* Number of OpenMP threads the parallel loops above use (1 without OpenMP). */
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    extern int omp_get_max_threads(void);
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
