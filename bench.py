@@ -1,0 +1,432 @@
+#!/usr/bin/env python3
+"""Benchmark: one verify pass of a 36-layer Qwen3-8B-shaped W8A8 stack.
+
+A step is one pass of the whole hot path over one batch of M tokens: for each
+of 36 layers, per-token activation quantisation of each linear's input and the
+seven linears (q, k, v, o, gate, up, down), then quantisation of the head input
+and the LM head with its greedy argmax.  Weights (7,568,097,280 bytes of int8,
+power-of-two scales) are generated from the seeded recipe, quantised on the
+GPU, and stay resident; the step reads all of them, which is far more than the
+L2 cache, so no explicit flush is needed.  Each linear gets its own synthetic
+bf16 activations (layers are not chained).
+
+`value` is weight GB/s over the step (weight codes + scales / step time) with
+the step captured as a CUDA graph; `e2e` is the same metric measured through
+the C-ABI entry points with the step's activations copied from pinned host
+memory and the argmax copied back inside the timed region.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--m M] [--impl reference]
+
+Under torchrun (N > 1) each rank runs an independent replica on its own GPU.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "W8A8 verify-pass linear weight GB/s & % of HBM roofline at M=1–8, bit-exact"
+UNIT = "GB/s"
+WORKLOAD = "qwen3_8b_stack36_verify_pass"
+
+# DRAM traffic of the weight-streaming kernel from one ncu capture (bytes read +
+# written per launch, scaled to the given launch) and the hash of the kernel
+# source it was taken on; reported only while the source is unchanged.
+NCU_TRAFFIC = {"source_sha256": None, "bytes_per_launch": None, "launch": None}
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--m", type=int, default=8, help="tokens per verify pass (1..16)")
+    p.add_argument("--layers", type=int, default=36)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--no-sweep", action="store_true", help="skip the per-M sweep")
+    return p.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def read_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples during the timed region (clocks and throttle reasons)."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(gpu_index), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            f = [c.strip() for c in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------- model
+
+class Stack:
+    """Resident int8 weights of the stack and per-step activation buffers."""
+
+    def __init__(self, bi, torch, layers: int, M: int, device):
+        import gen
+        self.bi, self.torch, self.M, self.dev = bi, torch, M, device
+        self.layers = layers
+        wl = gen.STACK36
+        self.lin = gen.QWEN3_8B_LINEARS
+        self.W = []       # per layer: dict name -> (wq, sw)
+        self.chunk = 8192
+        self.stage = torch.empty(self.chunk * 12288, dtype=torch.float32).pin_memory()
+        stage_np = self.stage.numpy()
+        for l in range(layers):
+            d = {}
+            for lin in self.lin:
+                d[lin.name] = self._make_weight(lambda r0, r, lin=lin, l=l: gen.weight_f32(
+                    wl.seed, l, lin.proj, lin.N, lin.K, row0=r0, rows=r, out=stage_np), lin.N, lin.K)
+            self.W.append(d)
+        # LM head with the planted near-tie rows for the head's activation rows
+        self.x_head_np = gen.activations(wl, 16, gen.LMHEAD.K, stream=7)
+        xh = self.x_head_np[:8]
+        self.head = self._make_weight(lambda r0, r: gen.lmhead_weight_f32(wl.seed, xh, r0, r, out=stage_np),
+                                      gen.LMHEAD.N, gen.LMHEAD.K)
+        del self.stage
+        self.weight_bytes = sum(l.N * l.K + 4 * l.N for l in self.lin) * layers + \
+            gen.LMHEAD.N * gen.LMHEAD.K + 4 * gen.LMHEAD.N
+        # activations: inputs of q/k/v, o, gate/up, down per layer, and the head
+        self.in_dims = [("qkv", 4096), ("o", 4096), ("gu", 4096), ("down", 12288)]
+        self.x_np = {}
+        self.x = {}
+        for l in range(layers):
+            for j, (nm, K) in enumerate(self.in_dims):
+                a = gen.activations(wl, 16, K, stream=100 + 4 * l + j)
+                self.x_np[(l, nm)] = a
+                self.x[(l, nm)] = torch.from_numpy(a.view(np.int16)).to(device)
+        self.x[("head",)] = torch.from_numpy(self.x_head_np.view(np.int16)).to(device)
+        self.x_np[("head",)] = self.x_head_np
+        self.ws = bi.new_workspace(16, 151936, 12288, device=device)
+        self.q = torch.empty((16, 12288), dtype=torch.int8, device=device)
+        self.s = torch.empty(16, dtype=torch.float32, device=device)
+        self.y = {lin.name: torch.empty((16, lin.N), dtype=torch.int16, device=device) for lin in self.lin}
+        self.argmax = torch.empty(16, dtype=torch.int32, device=device)
+        torch.cuda.synchronize()
+
+    def _make_weight(self, rows_fn, N, K):
+        torch, bi = self.torch, self.bi
+        wq = torch.empty((N, K), dtype=torch.int8, device=self.dev)
+        sw = torch.empty(N, dtype=torch.float32, device=self.dev)
+        for r0 in range(0, N, self.chunk):
+            r = min(self.chunk, N - r0)
+            rows_fn(r0, r)                      # fills the pinned staging buffer
+            w = self.stage[:r * K].view(r, K).to(self.dev, non_blocking=True)
+            bi.bi_quantize_weight(w, wq[r0:r0 + r], sw[r0:r0 + r])
+            bi.bi_requant_pow2(wq[r0:r0 + r], sw[r0:r0 + r], wq[r0:r0 + r], sw[r0:r0 + r])
+            torch.cuda.synchronize()
+        return wq, sw
+
+    def launches_per_step(self):
+        return self.layers * (len(self.in_dims) + len(self.lin)) + 2
+
+    def step(self, M, flags, timer=None):
+        """Enqueue one verify pass on the current stream.  timer(name, bytes)
+        returns a context that brackets one linear launch with events."""
+        bi, q, s = self.bi, self.q[:M], self.s[:M]
+        groups = {"qkv": ("q", "k", "v"), "o": ("o",), "gu": ("gate", "up"), "down": ("down",)}
+        for l in range(self.layers):
+            for nm, K in self.in_dims:
+                qbuf = self.q.view(-1)[:M * K].view(M, K)
+                bi.bi_quantize_act(self.x[(l, nm)][:M, :K], qbuf, s, K=K, flags=flags)
+                for pn in groups[nm]:
+                    wq, sw = self.W[l][pn]
+                    if timer is None:
+                        bi.bi_linear_w8a8(qbuf, s, wq, sw, self.y[pn][:M], self.ws, flags=flags)
+                    else:
+                        with timer(wq.shape[0] * K + 4 * wq.shape[0] + M * K + 4 * M + 2 * M * wq.shape[0]):
+                            bi.bi_linear_w8a8(qbuf, s, wq, sw, self.y[pn][:M], self.ws, flags=flags)
+        K = 4096
+        qbuf = self.q.view(-1)[:M * K].view(M, K)
+        bi.bi_quantize_act(self.x[("head",)][:M], qbuf, s, K=K, flags=flags)
+        wq, sw = self.head
+        bi.bi_lmhead_argmax(qbuf, s, wq, sw, None, self.argmax[:M], self.ws, flags=flags)
+
+
+def source_sha(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+def run_ours(args):
+    import torch
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import invariant_quantized_linear_gb300 as bi
+
+    M = args.m
+    assert 1 <= M <= 16
+    t0 = time.time()
+    st = Stack(bi, torch, args.layers, 16, dev)
+    setup_s = time.time() - t0
+    flags = bi.BI_FLAG_PDL
+    stream = torch.cuda.Stream(device=dev)
+
+    def barrier():
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    def graph_for(m):
+        with torch.cuda.stream(stream):
+            st.step(m, flags)          # warm-up outside capture (tensor maps, attributes)
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            st.step(m, flags)
+        return g
+
+    def time_graph(g, steps, warmup):
+        for _ in range(warmup):
+            g.replay()
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(steps):
+                g.replay()
+            e1.record(stream)
+        barrier()
+        ms = e0.elapsed_time(e1) / steps
+        if world > 1:
+            t = torch.tensor([ms], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            ms = float(t.item())
+        return ms
+
+    g = graph_for(M)
+    clocks = ClockSampler(local)
+    ms = time_graph(g, args.steps, args.warmup)
+    clk = clocks.stop()
+    gbs = st.weight_bytes * world / (ms * 1e-3) / 1e9
+
+    # per-M sweep (same step, fewer repetitions)
+    per_m = {}
+    if not args.no_sweep:
+        for m in (1, 2, 3, 4, 5, 8):
+            gm = g if m == M else graph_for(m)
+            msm = time_graph(gm, max(5, args.steps // 2), 3)
+            per_m[str(m)] = {"ms_per_step": round(msm, 4),
+                             "weight_gbs": round(st.weight_bytes / (msm * 1e-3) / 1e9, 1),
+                             "tokens_per_s_eq": round(m / (msm * 1e-3), 1)}
+
+    # dominant kernel: each weight-streaming launch of one pass bracketed by
+    # events on its stream (plain launches, no graph, no PDL)
+    durations, byts = [], []
+
+    class Timer:
+        def __init__(self, nbytes):
+            self.nbytes = nbytes
+
+        def __enter__(self):
+            self.a = torch.cuda.Event(enable_timing=True)
+            self.b = torch.cuda.Event(enable_timing=True)
+            self.a.record(stream)
+
+        def __exit__(self, *exc):
+            self.b.record(stream)
+            durations.append((self.a, self.b))
+            byts.append(self.nbytes)
+
+    with torch.cuda.stream(stream):
+        st.step(M, 0)
+        durations.clear()
+        byts.clear()
+        st.step(M, 0, timer=Timer)
+    stream.synchronize()
+    tot_ms = sum(a.elapsed_time(b) for a, b in durations)
+    achieved = sum(byts) / (tot_ms * 1e-3) / 1e9
+
+    # end to end: activations H2D from pinned memory, graph, argmax D2H
+    host_x = {k: torch.from_numpy(v.view(np.int16)).pin_memory() for k, v in st.x_np.items()}
+    host_am = torch.empty(16, dtype=torch.int32).pin_memory()
+    h2d = sum(int(v[:M].numel()) * 2 for v in host_x.values())
+    e2e_steps = max(3, args.steps // 2)
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            for k, v in host_x.items():
+                st.x[k][:M].copy_(v[:M], non_blocking=True)
+            g.replay()
+            host_am[:M].copy_(st.argmax[:M], non_blocking=True)
+        e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    e2e_gbs = st.weight_bytes * world / (e2e_ms * 1e-3) / 1e9
+
+    peaks, kind = read_peaks()
+    peak = float(peaks["hbm_gbs"])
+    skinny_src = os.path.join(ROOT, "invariant_quantized_linear_gb300", "csrc", "k_skinny.cu")
+    traffic = None
+    if NCU_TRAFFIC["source_sha256"] == source_sha(skinny_src):
+        traffic = NCU_TRAFFIC["bytes_per_launch"]
+
+    cpu = cpu_baseline(bounded_s=12.0) if rank == 0 else None
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(gbs, 1), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "int8", "data": "synthetic (seeded; fp32 N(0,0.02) weights -> absmax int8 -> pow2 scales; "
+                                     "bf16 N(0,1) activations)",
+            "config": {"workload": WORKLOAD, "M": M, "layers": args.layers, "hidden": 4096,
+                       "intermediate": 12288, "vocab": 151936, "weight_bytes_per_step": st.weight_bytes,
+                       "l2": "inputs larger than L2 (all weights read once per step)",
+                       "activations": "independent synthetic input per linear (layers not chained)",
+                       "launch": "CUDA graph of the step, programmatic dependent launch",
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "pct_of_hbm_copy": round(100 * gbs / world / peak, 1),
+            "tokens_per_s_eq": round(M * world / (ms * 1e-3), 1),
+            "per_m": per_m,
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "traffic": traffic,
+                         "kernel": "skinny_kernel (bi_linear_w8a8, M<=16)",
+                         "peak_kind": kind, "note": "achieved = algorithmic bytes (W + s_w + q + s_a + y) "
+                                                   "per launch / event-timed launch duration, summed over "
+                                                   "the 252 linear launches of one pass"},
+            "e2e": {"value": round(e2e_gbs, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": 4 * M, "ms_per_step": round(e2e_ms, 4)},
+            "gpu_launches": st.launches_per_step() * args.steps,
+            "clocks": clk,
+            "cpu_baseline": cpu,
+            "setup_s": round(setup_s, 1),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+def oracle_sample():
+    """A bounded sample of the workload for the CPU oracle: layer 0's q
+    projection (4096 x 4096) at M = 8, weights quantised by the oracle."""
+    import gen
+    import oracle
+    wl = gen.STACK36
+    lin = gen.QWEN3_8B_LINEARS[0]
+    w = gen.weight_f32(wl.seed, 0, lin.proj, lin.N, lin.K)
+    wq, sw = oracle.requant_pow2(*oracle.quantize_weight(w))
+    x = gen.activations(wl, 8, lin.K, stream=100)
+    return oracle, x, wq, sw, lin
+
+
+def cpu_baseline(bounded_s=12.0, M=8):
+    oracle, x, wq, sw, lin = oracle_sample()
+    t0 = time.time()
+    n = 0
+    while True:
+        q, s = oracle.quantize_act(x[:M])
+        oracle.linear_w8a8(q, s, wq, sw)
+        n += 1
+        if time.time() - t0 >= bounded_s:
+            break
+    dt = (time.time() - t0) / n
+    return {"value": round((lin.N * lin.K + 4 * lin.N) / dt / 1e9, 3), "unit": UNIT,
+            "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": "q projection of layer 0 (4096x4096 int8, pow2 scales) at M=%d, activation "
+                      "quantisation + linear, repeated %d times in %.1f s" % (M, n, time.time() - t0)}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    oracle, x, wq, sw, lin = oracle_sample()
+    M = args.m
+    for _ in range(args.warmup):
+        q, s = oracle.quantize_act(x[:M])
+        oracle.linear_w8a8(q, s, wq, sw)
+    t0 = time.time()
+    for _ in range(args.steps):
+        q, s = oracle.quantize_act(x[:M])
+        oracle.linear_w8a8(q, s, wq, sw)
+    dt = (time.time() - t0) / args.steps
+    v = (lin.N * lin.K + 4 * lin.N) / dt / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(v, 3), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8",
+            "data": "synthetic", "config": {"workload": WORKLOAD, "M": M},
+            "cpu_baseline": {"value": round(v, 3), "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": "one step = layer 0's 4096x4096 q projection at M=%d on the CPU oracle" % M},
+            "e2e": {"value": round(v, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    a = parse()
+    if a.impl == "reference":
+        run_reference(a)
+    else:
+        run_ours(a)

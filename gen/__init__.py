@@ -156,10 +156,13 @@ PREFILL = Workload("prefill", 4, True, True, (512, 2048))
 
 
 def weight_f32(seed: int, layer: int, proj: int, N: int, K: int, row0: int = 0,
-               rows: int | None = None) -> np.ndarray:
-    """Rows [row0, row0+rows) of an fp32 weight matrix W[N, K] ~ N(0, 0.02)."""
+               rows: int | None = None, out: np.ndarray | None = None) -> np.ndarray:
+    """Rows [row0, row0+rows) of an fp32 weight matrix W[N, K] ~ N(0, 0.02).
+    `out`, if given, is a float32 buffer of at least rows*K elements."""
     rows = N - row0 if rows is None else rows
-    flat = normal_f32(seed, weight_stream(layer, proj), rows * K, WEIGHT_SIGMA, offset=row0 * K)
+    if out is not None:
+        out = out.reshape(-1)[:rows * K]
+    flat = normal_f32(seed, weight_stream(layer, proj), rows * K, WEIGHT_SIGMA, offset=row0 * K, out=out)
     return flat.reshape(rows, K)
 
 
@@ -188,11 +191,11 @@ def lmhead_special_rows(N: int) -> dict:
 
 
 def lmhead_weight_f32(seed: int, x_bf16: np.ndarray, row0: int, rows: int,
-                      N: int = LMHEAD.N, K: int = LMHEAD.K) -> np.ndarray:
+                      N: int = LMHEAD.N, K: int = LMHEAD.K, out: np.ndarray | None = None) -> np.ndarray:
     """Rows [row0, row0+rows) of the LM-head weights, near-tie rows included.
 
     x_bf16 holds the (up to 8) activation rows the ties are planted for."""
-    W = weight_f32(seed, 0, LMHEAD.proj, N, K, row0=row0, rows=rows)
+    W = weight_f32(seed, 0, LMHEAD.proj, N, K, row0=row0, rows=rows, out=out)
     xs = bf16_bits_to_f32(x_bf16[:, :K])
     mag = np.abs(normal_f32(seed, 9, 8 * K, WEIGHT_SIGMA).reshape(8, K))
     for m, (a, b) in lmhead_special_rows(N).items():

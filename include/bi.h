@@ -1,0 +1,176 @@
+/*
+ * bi.h - batch-invariant W8A8 linear layer for GB300 (sm_103a), C ABI.
+ *
+ * The library computes the linear layers of an LLM decode or speculative
+ * verify pass (M = 1 .. K+1 tokens against a large int8 weight matrix) so that
+ * every output row is bitwise identical whatever M is and whatever else shares
+ * the pass.  Greedy speculative decoding then keeps exactly the target's own
+ * argmax ("why speculative decoding changed my output", introduction: the
+ * guarantee needs a position's logits inside a batch to equal its logits
+ * decoded alone).
+ *
+ * Arithmetic (W8A8 as in "Deterministic LLM Inference Across GPU Kernels:
+ * Power-of-Two INT8 Quantization Scales and the Limits of Tolerance-Based
+ * Conformance", Abstract, Fig. 1, Table II):
+ *   s_a[m]   = absmax_k |x[m,k]| / 127  (IEEE fp32 division; 1 if absmax = 0)
+ *   q[m,k]   = clamp(rne(x[m,k] / s_a[m]), -127, 127)
+ *   acc[m,n] = sum_k q[m,k] * W[n,k]       exact in int32 (K * 127^2 < 2^31)
+ *   y[m,n]   = bf16_rne((float(acc) * s_a[m]) * s_w[n])
+ * The integer sum is exact and independent of summation order ("The Integer
+ * Alibi", abstract), so the kernels may split K in any way; the epilogue is
+ * fixed element by element.  Hence rows do not depend on M.
+ *
+ * Conventions for every entry point:
+ *  - Pointers are DEVICE pointers, allocated and owned by the caller; the
+ *    library allocates nothing and keeps no pointer after returning.
+ *  - bf16 values are passed as their uint16_t bit patterns.
+ *  - Matrices are row-major: x [M, ldx] (ldx >= K), q [M, K], W [N, K]
+ *    (K contiguous), y / logits [M, N].
+ *  - Work is enqueued on `stream` (NULL = legacy default stream) and the call
+ *    returns without waiting.  Calls are reentrant; calls that may run
+ *    concurrently on the device must not share output or workspace buffers.
+ *  - Arguments are validated on the host before anything is launched; an
+ *    invalid call returns an error status and enqueues nothing.  No call
+ *    aborts, throws, or writes to stderr.
+ *  - Shape limits: 1 <= M <= 65535, 1 <= N <= 2^31-1, 16 <= K, K % 16 == 0,
+ *    K * 127^2 < 2^31 (K <= 133144).  Base pointers of x, q and w_q must be
+ *    16-byte aligned, and ldx % 8 == 0 (16-byte aligned rows).
+ */
+#ifndef BI_H
+#define BI_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define BI_API __attribute__((visibility("default")))
+#else
+#define BI_API
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *bi_stream_t;
+
+typedef enum {
+    BI_OK = 0,
+    BI_ERR_INVALID_ARG = 1, /* null pointer, bad shape, ldx < K, K % 16 != 0 */
+    BI_ERR_ALIGNMENT = 2,   /* a base pointer or row stride not 16-byte aligned */
+    BI_ERR_INT32_BOUND = 3, /* K * 127^2 >= 2^31: the int32 sum could overflow */
+    BI_ERR_WORKSPACE = 4,   /* workspace null or smaller than the queried size */
+    BI_ERR_UNSUPPORTED = 5, /* no usable sm_103a device, or a feature missing */
+    BI_ERR_TIMEOUT = 6,     /* a kernel gave up a bounded wait (see bi_workspace_status) */
+    BI_ERR_CUDA = 7         /* a CUDA runtime/driver call failed */
+} bi_status;
+
+/* Flags for the calls that take `flags`. */
+enum {
+    /* Programmatic dependent launch.  The call may begin while the kernel
+     * that precedes it on `stream` is still running: it waits for that kernel
+     * before reading any of its inputs except the weight codes w_q, which it
+     * may start streaming early, and it lets the next kernel on the stream
+     * launch early in the same way.  Use it only when w_q is not written by
+     * the immediately preceding kernel (weights are constants of the model).
+     * Results are bitwise identical with and without the flag. */
+    BI_FLAG_PDL = 1u
+};
+
+/* Human-readable name of a status (static string, never NULL). */
+BI_API const char *bi_status_string(bi_status s);
+
+/*
+ * Per-token activation quantisation.
+ *   x    bf16 [M, ldx], first K columns used (read only)
+ *   q    int8 [M, K] out, s_a fp32 [M] out
+ * s_a[m] = absmax/127 by IEEE division (1 for an all-zero row); q by IEEE
+ * division x/s_a, round-to-nearest-even, clamp to [-127, 127].  Subnormal
+ * inputs are honoured (no flush to zero).  With BI_FLAG_PDL the kernel waits
+ * for the preceding kernel before reading x.
+ */
+BI_API bi_status bi_quantize_act(const uint16_t *x, int64_t ldx, int M, int K,
+                          int8_t *q, float *s_a, unsigned flags, bi_stream_t stream);
+
+/*
+ * Checkpoint-style per-output-channel weight quantisation (offline, not part
+ * of the verify pass): the same rule as bi_quantize_act applied to each row of
+ * an fp32 matrix.
+ *   w    fp32 [N, ldw] (ldw >= K, ldw % 4 == 0, 16-byte aligned), read only
+ *   w_q  int8 [N, K] out, s_w fp32 [N] out
+ */
+BI_API bi_status bi_quantize_weight(const float *w, int64_t ldw, int N, int K,
+                             int8_t *w_q, float *s_w, bi_stream_t stream);
+
+/*
+ * Power-of-two scale requantisation ("Deterministic LLM Inference ...",
+ * Abstract and Fig. 1: every weight scale is moved to its nearest power of
+ * two and the codes are requantised to it, not merely relabelled).
+ *   s'   = 2^round(log2 s_w[n])   (nearest in the log domain; never a tie)
+ *   w_q' = clamp(rne(w_q * s_w[n] / s'), -127, 127), computed exactly
+ * A scale whose power of two would exceed fp32 is held at 2^127; rows whose
+ * scale is not a positive finite number are copied unchanged.  Outputs may
+ * alias the inputs exactly (w_q_out == w_q, s_w_out == s_w) for an in-place
+ * update; partial overlap is not allowed.
+ */
+BI_API bi_status bi_requant_pow2(const int8_t *w_q, const float *s_w, int N, int K,
+                          int8_t *w_q_out, float *s_w_out, bi_stream_t stream);
+
+/*
+ * Workspace bytes needed by bi_linear_w8a8 for this shape (> 0).  The
+ * workspace holds split-K partial sums, their counters and a status word.  It
+ * must be zero-filled before its first use (cudaMemset); every call that
+ * completes leaves it zero-filled again, so one workspace can serve a whole
+ * sequence of calls on one stream.
+ */
+BI_API size_t bi_linear_workspace_size(int M, int N, int K);
+
+/*
+ * y = the W8A8 linear layer above.
+ *   q    int8 [M, K], s_a fp32 [M]          (from bi_quantize_act)
+ *   w_q  int8 [N, K], s_w fp32 [N]          (per-output-channel codes/scales)
+ *   y    bf16 [M, N] out (row stride N)
+ *   ws   workspace of ws_bytes >= bi_linear_workspace_size(M, N, K)
+ * M <= 16 runs the weight-streaming kernel (TMA-staged int8 weight tiles,
+ * int8 tensor-core dot products, int32 partial sums reduced exactly across
+ * CTAs); larger M runs the tiled prefill kernel.  Both give the same bits for
+ * every row.  Any outputs that do not fit bf16 become +-Inf by round to
+ * nearest even.
+ */
+BI_API bi_status bi_linear_w8a8(const int8_t *q, const float *s_a, int M, int K,
+                         const int8_t *w_q, const float *s_w, int N,
+                         uint16_t *y, void *ws, size_t ws_bytes,
+                         unsigned flags, bi_stream_t stream);
+
+/* Workspace bytes needed by bi_lmhead_argmax (same zero-fill rule). */
+BI_API size_t bi_lmhead_workspace_size(int M, int N, int K);
+
+/*
+ * Greedy LM head: the logits of bi_linear_w8a8 (optionally written to
+ * `logits`, bf16 [M, N]) and, per row, argmax[m] = the lowest n whose bf16
+ * logit is the row maximum, logits compared as real numbers (-0 == +0).
+ * ("My speculative decoder got slower", "We're nowhere near SOL": a head that
+ * computes only the winning token; "Why the decoders disagreed?": bf16 logits
+ * do tie.)  M <= 16.
+ *   logits  bf16 [M, N] out, or NULL to skip writing them
+ *   argmax  int32 [M] out
+ */
+BI_API bi_status bi_lmhead_argmax(const int8_t *q, const float *s_a, int M, int K,
+                           const int8_t *w_q, const float *s_w, int N,
+                           uint16_t *logits, int32_t *argmax,
+                           void *ws, size_t ws_bytes, unsigned flags, bi_stream_t stream);
+
+/*
+ * Device-side status of a workspace: waits for `stream`, reads the status word
+ * that kernels set when a bounded wait gives up, clears it, and returns BI_OK
+ * or BI_ERR_TIMEOUT (or BI_ERR_CUDA if the stream itself reports an error).
+ * After BI_ERR_TIMEOUT the workspace must be zero-filled again before reuse.
+ */
+BI_API bi_status bi_workspace_status(void *ws, size_t ws_bytes, bi_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BI_H */

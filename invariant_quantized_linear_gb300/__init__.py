@@ -1,0 +1,140 @@
+"""Batch-invariant W8A8 linear layer for GB300 (sm_103a): Python binding.
+
+A thin ctypes layer over ``libbi.so`` (C ABI declared in ``include/bi.h``).
+Each function has the name of the C entry point it calls and only marshals
+arguments: tensor pointers, shapes and the current CUDA stream.  All
+arithmetic runs in the library's CUDA kernels; there is no other code path.
+If ``libbi.so`` is missing or fails to load, importing this package raises.
+
+PyTorch supplies device memory and streams.  bf16 tensors may be passed as
+``torch.bfloat16`` or as their ``int16``/``uint16`` bit patterns.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libbi.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError("libbi.so is not built: run invariant_quantized_linear_gb300/build.py "
+                      "(or __graft_entry__.build()) first")
+
+lib = ctypes.CDLL(LIB_PATH)
+
+_vp, _i64, _ci, _cu, _sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint, ctypes.c_size_t
+lib.bi_status_string.argtypes = [_ci]
+lib.bi_status_string.restype = ctypes.c_char_p
+lib.bi_quantize_act.argtypes = [_vp, _i64, _ci, _ci, _vp, _vp, _cu, _vp]
+lib.bi_quantize_act.restype = _ci
+lib.bi_quantize_weight.argtypes = [_vp, _i64, _ci, _ci, _vp, _vp, _vp]
+lib.bi_quantize_weight.restype = _ci
+lib.bi_requant_pow2.argtypes = [_vp, _vp, _ci, _ci, _vp, _vp, _vp]
+lib.bi_requant_pow2.restype = _ci
+lib.bi_linear_workspace_size.argtypes = [_ci, _ci, _ci]
+lib.bi_linear_workspace_size.restype = _sz
+lib.bi_lmhead_workspace_size.argtypes = [_ci, _ci, _ci]
+lib.bi_lmhead_workspace_size.restype = _sz
+lib.bi_linear_w8a8.argtypes = [_vp, _vp, _ci, _ci, _vp, _vp, _ci, _vp, _vp, _sz, _cu, _vp]
+lib.bi_linear_w8a8.restype = _ci
+lib.bi_lmhead_argmax.argtypes = [_vp, _vp, _ci, _ci, _vp, _vp, _ci, _vp, _vp, _vp, _sz, _cu, _vp]
+lib.bi_lmhead_argmax.restype = _ci
+lib.bi_workspace_status.argtypes = [_vp, _sz, _vp]
+lib.bi_workspace_status.restype = _ci
+
+BI_OK = 0
+BI_ERR_INVALID_ARG = 1
+BI_ERR_ALIGNMENT = 2
+BI_ERR_INT32_BOUND = 3
+BI_ERR_WORKSPACE = 4
+BI_ERR_UNSUPPORTED = 5
+BI_ERR_TIMEOUT = 6
+BI_ERR_CUDA = 7
+BI_FLAG_PDL = 1
+
+
+class BiError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__("%s: %s" % (what, lib.bi_status_string(status).decode()))
+
+
+def _check(status: int, what: str) -> None:
+    if status != BI_OK:
+        raise BiError(status, what)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def bi_status_string(status: int) -> str:
+    return lib.bi_status_string(status).decode()
+
+
+def bi_quantize_act(x: torch.Tensor, q: torch.Tensor, s_a: torch.Tensor, K: int | None = None,
+                    flags: int = 0, stream=None) -> None:
+    """x: bf16 [M, ldx] (row stride ldx = x.stride(0)); q: int8 [M, K]; s_a: fp32 [M]."""
+    M = x.shape[0]
+    K = x.shape[1] if K is None else K
+    _check(lib.bi_quantize_act(_ptr(x), x.stride(0), M, K, _ptr(q), _ptr(s_a), flags, _stream(stream)),
+           "bi_quantize_act")
+
+
+def bi_quantize_weight(w: torch.Tensor, w_q: torch.Tensor, s_w: torch.Tensor, stream=None) -> None:
+    N, K = w.shape
+    _check(lib.bi_quantize_weight(_ptr(w), w.stride(0), N, K, _ptr(w_q), _ptr(s_w), _stream(stream)),
+           "bi_quantize_weight")
+
+
+def bi_requant_pow2(w_q: torch.Tensor, s_w: torch.Tensor, w_q_out: torch.Tensor, s_w_out: torch.Tensor,
+                    stream=None) -> None:
+    N, K = w_q.shape
+    _check(lib.bi_requant_pow2(_ptr(w_q), _ptr(s_w), N, K, _ptr(w_q_out), _ptr(s_w_out), _stream(stream)),
+           "bi_requant_pow2")
+
+
+def bi_linear_workspace_size(M: int, N: int, K: int) -> int:
+    return int(lib.bi_linear_workspace_size(M, N, K))
+
+
+def bi_lmhead_workspace_size(M: int, N: int, K: int) -> int:
+    return int(lib.bi_lmhead_workspace_size(M, N, K))
+
+
+def bi_linear_w8a8(q: torch.Tensor, s_a: torch.Tensor, w_q: torch.Tensor, s_w: torch.Tensor,
+                   y: torch.Tensor, ws: torch.Tensor, flags: int = 0, stream=None) -> None:
+    M, K = q.shape
+    N = w_q.shape[0]
+    _check(lib.bi_linear_w8a8(_ptr(q), _ptr(s_a), M, K, _ptr(w_q), _ptr(s_w), N, _ptr(y), _ptr(ws),
+                              ws.numel() * ws.element_size(), flags, _stream(stream)), "bi_linear_w8a8")
+
+
+def bi_lmhead_argmax(q: torch.Tensor, s_a: torch.Tensor, w_q: torch.Tensor, s_w: torch.Tensor,
+                     logits: torch.Tensor | None, argmax: torch.Tensor, ws: torch.Tensor,
+                     flags: int = 0, stream=None) -> None:
+    M, K = q.shape
+    N = w_q.shape[0]
+    _check(lib.bi_lmhead_argmax(_ptr(q), _ptr(s_a), M, K, _ptr(w_q), _ptr(s_w), N, _ptr(logits),
+                                _ptr(argmax), _ptr(ws), ws.numel() * ws.element_size(), flags,
+                                _stream(stream)), "bi_lmhead_argmax")
+
+
+def bi_workspace_status(ws: torch.Tensor, stream=None) -> int:
+    """BI_OK or BI_ERR_TIMEOUT (returned, not raised); clears the status word."""
+    return int(lib.bi_workspace_status(_ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def new_workspace(M: int, N: int, K: int, device="cuda") -> torch.Tensor:
+    """A zero-filled workspace large enough for bi_linear_w8a8 and bi_lmhead_argmax."""
+    n = max(bi_linear_workspace_size(M, N, K), bi_lmhead_workspace_size(M, N, K))
+    return torch.zeros(n, dtype=torch.uint8, device=device)

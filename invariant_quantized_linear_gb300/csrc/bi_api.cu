@@ -1,0 +1,263 @@
+// C ABI of the batch-invariant W8A8 library: argument validation, TMA
+// descriptor encoding and kernel dispatch.  Declarations and the contract of
+// every entry point are in include/bi.h.
+#include "bi.h"
+#include "kernels.cuh"
+#include "ptx.cuh"
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+namespace {
+
+using bi::kMaxGrid;
+
+constexpr long long kMaxK = 133144;  // largest K with K * 127^2 < 2^31
+
+bool aligned16(const void *p)
+{
+    return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+bool aligned4(const void *p)
+{
+    return (reinterpret_cast<uintptr_t>(p) & 3u) == 0;
+}
+
+bi_status from_cuda(cudaError_t e)
+{
+    return e == cudaSuccess ? BI_OK : BI_ERR_CUDA;
+}
+
+// K range shared by every entry point.
+bi_status check_k(int K)
+{
+    if (K < 16 || (K % 16) != 0) return BI_ERR_INVALID_ARG;
+    if (static_cast<long long>(K) > kMaxK) return BI_ERR_INT32_BOUND;
+    return BI_OK;
+}
+
+// The library is built for sm_103a only.
+bi_status device_info(int *sm_count)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return BI_ERR_UNSUPPORTED;
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+        return BI_ERR_UNSUPPORTED;
+    if (major != 10 || minor != 3) return BI_ERR_UNSUPPORTED;
+    if (sm_count) {
+        if (cudaDeviceGetAttribute(sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return BI_ERR_UNSUPPORTED;
+    }
+    return BI_OK;
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point, so the
+// library does not link libcuda directly.
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// 2-D int8 tensor [rows, cols] (row stride cols bytes), box box_cols x box_rows,
+// 128-byte swizzle, zero fill outside the tensor.
+bi_status encode_int8_2d(CUtensorMap *map, const void *base, long long rows, long long cols, int box_cols,
+                         int box_rows, bool stream_once)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return BI_ERR_UNSUPPORTED;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    stream_once ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B : CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? BI_OK : BI_ERR_CUDA;
+}
+
+bi_status check_linear_args(const int8_t *q, const float *s_a, int M, int K, const int8_t *w_q, const float *s_w,
+                            int N, void *ws, size_t ws_bytes)
+{
+    if (!q || !s_a || !w_q || !s_w) return BI_ERR_INVALID_ARG;
+    if (M < 1 || M > 65535 || N < 1) return BI_ERR_INVALID_ARG;
+    bi_status s = check_k(K);
+    if (s != BI_OK) return s;
+    if (!aligned16(q) || !aligned16(w_q) || !aligned4(s_a) || !aligned4(s_w)) return BI_ERR_ALIGNMENT;
+    if (!ws || ws_bytes < bi::kWsBytes || !aligned16(ws)) return BI_ERR_WORKSPACE;
+    return BI_OK;
+}
+
+bi_status run_skinny(const int8_t *q, const float *s_a, int M, int K, const int8_t *w_q, const float *s_w, int N,
+                     uint16_t *y, int32_t *argmax, void *ws, unsigned flags, cudaStream_t stream)
+{
+    int sms = 0;
+    bi_status st = device_info(&sms);
+    if (st != BI_OK) return st;
+    bi::SkinnyArgs a;
+    const int tok_rows = M > 8 ? 16 : 8;
+    st = encode_int8_2d(&a.map_w, w_q, N, K, 128, bi::kBM, true);
+    if (st != BI_OK) return st;
+    st = encode_int8_2d(&a.map_q, q, M, K, 128, tok_rows, false);
+    if (st != BI_OK) return st;
+    a.s_a = s_a;
+    a.s_w = s_w;
+    a.y = y;
+    a.argmax = argmax;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.ws = bi::workspace_view(ws);
+    a.pdl = (flags & BI_FLAG_PDL) != 0;
+    a.grid = sms < kMaxGrid ? sms : kMaxGrid;
+    return from_cuda(bi::launch_skinny(a, stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *bi_status_string(bi_status s)
+{
+    switch (s) {
+    case BI_OK: return "BI_OK";
+    case BI_ERR_INVALID_ARG: return "BI_ERR_INVALID_ARG: null pointer or invalid shape";
+    case BI_ERR_ALIGNMENT: return "BI_ERR_ALIGNMENT: pointer or row stride not 16-byte aligned";
+    case BI_ERR_INT32_BOUND: return "BI_ERR_INT32_BOUND: K * 127^2 >= 2^31";
+    case BI_ERR_WORKSPACE: return "BI_ERR_WORKSPACE: workspace missing or too small";
+    case BI_ERR_UNSUPPORTED: return "BI_ERR_UNSUPPORTED: no sm_103a device or missing driver feature";
+    case BI_ERR_TIMEOUT: return "BI_ERR_TIMEOUT: a kernel gave up a bounded wait";
+    case BI_ERR_CUDA: return "BI_ERR_CUDA: a CUDA call failed";
+    }
+    return "unknown bi_status";
+}
+
+bi_status bi_quantize_act(const uint16_t *x, int64_t ldx, int M, int K, int8_t *q, float *s_a, unsigned flags,
+                          bi_stream_t stream)
+{
+    if (!x || !q || !s_a) return BI_ERR_INVALID_ARG;
+    if (M < 1 || M > 65535 || ldx < K) return BI_ERR_INVALID_ARG;
+    bi_status st = check_k(K);
+    if (st != BI_OK) return st;
+    if (!aligned16(x) || !aligned16(q) || !aligned4(s_a) || (ldx % 8) != 0) return BI_ERR_ALIGNMENT;
+    st = device_info(nullptr);
+    if (st != BI_OK) return st;
+    return from_cuda(bi::launch_quantize_act(x, ldx, M, K, q, s_a, (flags & BI_FLAG_PDL) != 0, stream));
+}
+
+bi_status bi_quantize_weight(const float *w, int64_t ldw, int N, int K, int8_t *w_q, float *s_w, bi_stream_t stream)
+{
+    if (!w || !w_q || !s_w) return BI_ERR_INVALID_ARG;
+    if (N < 1 || ldw < K) return BI_ERR_INVALID_ARG;
+    bi_status st = check_k(K);
+    if (st != BI_OK) return st;
+    if (!aligned16(w) || !aligned16(w_q) || !aligned4(s_w) || (ldw % 4) != 0) return BI_ERR_ALIGNMENT;
+    st = device_info(nullptr);
+    if (st != BI_OK) return st;
+    return from_cuda(bi::launch_quantize_weight(w, ldw, N, K, w_q, s_w, stream));
+}
+
+bi_status bi_requant_pow2(const int8_t *w_q, const float *s_w, int N, int K, int8_t *w_q_out, float *s_w_out,
+                          bi_stream_t stream)
+{
+    if (!w_q || !s_w || !w_q_out || !s_w_out || N < 1) return BI_ERR_INVALID_ARG;
+    bi_status st = check_k(K);
+    if (st != BI_OK) return st;
+    if (!aligned16(w_q) || !aligned16(w_q_out) || !aligned4(s_w) || !aligned4(s_w_out)) return BI_ERR_ALIGNMENT;
+    // exact aliasing is allowed, partial overlap is not
+    const size_t wbytes = static_cast<size_t>(N) * static_cast<size_t>(K);
+    const char *a = reinterpret_cast<const char *>(w_q), *b = reinterpret_cast<const char *>(w_q_out);
+    if (a != b && a < b + wbytes && b < a + wbytes) return BI_ERR_INVALID_ARG;
+    const char *c = reinterpret_cast<const char *>(s_w), *d = reinterpret_cast<const char *>(s_w_out);
+    const size_t sbytes = static_cast<size_t>(N) * sizeof(float);
+    if (c != d && c < d + sbytes && d < c + sbytes) return BI_ERR_INVALID_ARG;
+    st = device_info(nullptr);
+    if (st != BI_OK) return st;
+    return from_cuda(bi::launch_requant_pow2(w_q, s_w, N, K, w_q_out, s_w_out, stream));
+}
+
+size_t bi_linear_workspace_size(int M, int N, int K)
+{
+    (void)M;
+    (void)N;
+    (void)K;
+    return bi::kWsBytes;
+}
+
+size_t bi_lmhead_workspace_size(int M, int N, int K)
+{
+    (void)M;
+    (void)N;
+    (void)K;
+    return bi::kWsBytes;
+}
+
+bi_status bi_linear_w8a8(const int8_t *q, const float *s_a, int M, int K, const int8_t *w_q, const float *s_w, int N,
+                         uint16_t *y, void *ws, size_t ws_bytes, unsigned flags, bi_stream_t stream)
+{
+    bi_status st = check_linear_args(q, s_a, M, K, w_q, s_w, N, ws, ws_bytes);
+    if (st != BI_OK) return st;
+    if (!y) return BI_ERR_INVALID_ARG;
+    if (M <= 16) return run_skinny(q, s_a, M, K, w_q, s_w, N, y, nullptr, ws, flags, stream);
+
+    st = device_info(nullptr);
+    if (st != BI_OK) return st;
+    bi::PrefillArgs a;
+    st = encode_int8_2d(&a.map_w, w_q, N, K, 128, 128, false);
+    if (st != BI_OK) return st;
+    st = encode_int8_2d(&a.map_q, q, M, K, 128, 128, false);
+    if (st != BI_OK) return st;
+    a.s_a = s_a;
+    a.s_w = s_w;
+    a.y = y;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.ws = bi::workspace_view(ws);
+    a.pdl = (flags & BI_FLAG_PDL) != 0;
+    return from_cuda(bi::launch_prefill(a, stream));
+}
+
+bi_status bi_lmhead_argmax(const int8_t *q, const float *s_a, int M, int K, const int8_t *w_q, const float *s_w,
+                           int N, uint16_t *logits, int32_t *argmax, void *ws, size_t ws_bytes, unsigned flags,
+                           bi_stream_t stream)
+{
+    bi_status st = check_linear_args(q, s_a, M, K, w_q, s_w, N, ws, ws_bytes);
+    if (st != BI_OK) return st;
+    if (!argmax || M > 16) return BI_ERR_INVALID_ARG;
+    if (!aligned4(argmax)) return BI_ERR_ALIGNMENT;
+    return run_skinny(q, s_a, M, K, w_q, s_w, N, logits, argmax, ws, flags, stream);
+}
+
+bi_status bi_workspace_status(void *ws, size_t ws_bytes, bi_stream_t stream)
+{
+    if (!ws || ws_bytes < bi::kWsBytes) return BI_ERR_WORKSPACE;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return BI_ERR_CUDA;
+    int word = 0;
+    if (cudaMemcpy(&word, ws, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return BI_ERR_CUDA;
+    if (word == bi::DEV_OK) return BI_OK;
+    const int zero = 0;
+    if (cudaMemcpy(ws, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return BI_ERR_CUDA;
+    return BI_ERR_TIMEOUT;
+}
+
+}  // extern "C"

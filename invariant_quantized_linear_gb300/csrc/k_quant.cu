@@ -1,0 +1,219 @@
+// Row-wise quantisation kernels: per-token activation quantisation (bf16 in),
+// checkpoint-style weight quantisation (fp32 in) and power-of-two scale
+// requantisation of int8 weights.
+//
+// Arithmetic follows the W8A8 pipeline of "Deterministic LLM Inference Across
+// GPU Kernels: Power-of-Two INT8 Quantization Scales and the Limits of
+// Tolerance-Based Conformance" (Abstract, Fig. 1): s = absmax/127 by IEEE
+// division, q = clamp(rne(v/s), -127, 127); power-of-two scales are built by
+// requantising the codes, not by rewriting the scales.
+#include "kernels.cuh"
+#include "ptx.cuh"
+
+namespace bi {
+
+namespace {
+
+constexpr int kQuantThreads = 256;
+
+__device__ __forceinline__ float block_max(float v, float *red)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        v = (lane < kQuantThreads / 32) ? red[lane] : 0.0f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+        if (lane == 0) red[0] = v;
+    }
+    __syncthreads();
+    return red[0];
+}
+
+__device__ __forceinline__ int8_t quant1(float v, float s)
+{
+    int r = __float2int_rn(__fdiv_rn(v, s));  // IEEE division, round half to even
+    r = max(-127, min(127, r));
+    return static_cast<int8_t>(r);
+}
+
+// Load 16 consecutive elements of a row as fp32 (exact widening for bf16).
+template <bool BF16>
+__device__ __forceinline__ void load16(const void *row, int k, float (&v)[16])
+{
+    if constexpr (BF16) {
+        const uint4 *p = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(row) + k);
+        uint4 a = p[0], b = p[1];
+        const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            v[2 * i] = __uint_as_float(w[i] << 16);
+            v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        }
+    } else {
+        const float4 *p = reinterpret_cast<const float4 *>(static_cast<const float *>(row) + k);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float4 t = p[i];
+            v[4 * i] = t.x;
+            v[4 * i + 1] = t.y;
+            v[4 * i + 2] = t.z;
+            v[4 * i + 3] = t.w;
+        }
+    }
+}
+
+// One CTA per row.  Pass 1: absmax (exact; max is order-free).  Pass 2:
+// quantise 16 elements per thread per step and store them as one 16-byte word.
+template <bool BF16>
+__global__ void __launch_bounds__(kQuantThreads) quantize_rows_kernel(const void *__restrict__ x, int64_t ld,
+                                                                      int K, int8_t *__restrict__ q,
+                                                                      float *__restrict__ s_out, int pdl)
+{
+    __shared__ float red[kQuantThreads / 32];
+    if (pdl) {
+        pdl_launch_dependents();
+        pdl_wait();
+    }
+    const int64_t row = blockIdx.x;
+    const size_t esz = BF16 ? 2 : 4;
+    const void *xr = static_cast<const char *>(x) + row * ld * esz;
+
+    float amax = 0.0f;
+    for (int k = threadIdx.x * 16; k < K; k += kQuantThreads * 16) {
+        float v[16];
+        load16<BF16>(xr, k, v);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    }
+    amax = block_max(amax, red);
+    const float s = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 127.0f);
+
+    int8_t *qr = q + row * K;
+    for (int k = threadIdx.x * 16; k < K; k += kQuantThreads * 16) {
+        float v[16];
+        load16<BF16>(xr, k, v);
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            uint32_t b0 = static_cast<uint8_t>(quant1(v[4 * i], s));
+            uint32_t b1 = static_cast<uint8_t>(quant1(v[4 * i + 1], s));
+            uint32_t b2 = static_cast<uint8_t>(quant1(v[4 * i + 2], s));
+            uint32_t b3 = static_cast<uint8_t>(quant1(v[4 * i + 3], s));
+            w[i] = b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
+        }
+        *reinterpret_cast<uint4 *>(qr + k) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    if (threadIdx.x == 0) s_out[row] = s;
+}
+
+// Round the integer p / 2^sh to nearest, ties to even (sh >= 1), symmetric in sign.
+__device__ __forceinline__ int64_t rne_shift(int64_t p, int sh)
+{
+    const bool neg = p < 0;
+    uint64_t a = static_cast<uint64_t>(neg ? -p : p);
+    uint64_t fl = a >> sh;
+    uint64_t rem = a & ((1ull << sh) - 1);
+    uint64_t half = 1ull << (sh - 1);
+    if (rem > half || (rem == half && (fl & 1ull))) ++fl;
+    return neg ? -static_cast<int64_t>(fl) : static_cast<int64_t>(fl);
+}
+
+// One CTA per row.  The scale s = mant * 2^(e - 150) (mant a 24-bit integer
+// with its top bit set, after normalising subnormals) has frexp form
+// m = mant / 2^24 in [0.5, 1), E = e - 126.  Its nearest power of two in the
+// log domain is 2^E when m^2 >= 1/2, i.e. mant^2 >= 2^47 (exact in 64 bits),
+// else 2^(E-1).  The new code is q * s / s' = q * mant / 2^(24 - (E - e2)),
+// an integer divided by a power of two, rounded half to even and clamped.
+__global__ void __launch_bounds__(kQuantThreads) requant_pow2_kernel(const int8_t *w_q, const float *s_w, int K,
+                                                                     int8_t *w_q_out, float *s_w_out)
+{
+    __shared__ float s_sh;
+    const int64_t row = blockIdx.x;
+    if (threadIdx.x == 0) s_sh = s_w[row];
+    __syncthreads();
+    const float s = s_sh;
+    const int8_t *src = w_q + row * K;
+    int8_t *dst = w_q_out + row * K;
+    const uint32_t bits = __float_as_uint(s);
+    const bool usable = (s > 0.0f) && (((bits >> 23) & 0xFFu) != 0xFFu);
+
+    float s_new = s;
+    if (usable) {
+        int e = static_cast<int>((bits >> 23) & 0xFFu);
+        uint32_t mant = bits & 0x7FFFFFu;
+        if (e == 0) {  // subnormal: normalise so bit 23 is set
+            int lz = __clz(mant) - 8;
+            mant <<= lz;
+            e = 1 - lz;
+        } else {
+            mant |= 0x800000u;
+        }
+        const int E = e - 126;
+        const uint64_t m2 = static_cast<uint64_t>(mant) * mant;
+        int e2 = (m2 >= (1ull << 47)) ? E : E - 1;
+        if (e2 > 127) e2 = 127;
+        const int sh = 24 - (E - e2);  // 24 or 23
+        s_new = (e2 >= -126) ? __uint_as_float(static_cast<uint32_t>(e2 + 127) << 23)
+                             : __uint_as_float(1u << (e2 + 149));
+        for (int k = threadIdx.x * 16; k < K; k += kQuantThreads * 16) {
+            uint4 in = *reinterpret_cast<const uint4 *>(src + k);
+            uint32_t wv[4] = {in.x, in.y, in.z, in.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                uint32_t o = 0;
+#pragma unroll
+                for (int b = 0; b < 4; ++b) {
+                    int c = static_cast<int8_t>((wv[i] >> (8 * b)) & 0xFFu);
+                    int64_t r = rne_shift(static_cast<int64_t>(c) * mant, sh);
+                    r = r > 127 ? 127 : (r < -127 ? -127 : r);
+                    o |= (static_cast<uint32_t>(r) & 0xFFu) << (8 * b);
+                }
+                wv[i] = o;
+            }
+            *reinterpret_cast<uint4 *>(dst + k) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+        }
+    } else if (dst != src) {
+        for (int k = threadIdx.x * 16; k < K; k += kQuantThreads * 16)
+            *reinterpret_cast<uint4 *>(dst + k) = *reinterpret_cast<const uint4 *>(src + k);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) s_w_out[row] = s_new;
+}
+
+}  // namespace
+
+cudaError_t launch_quantize_act(const uint16_t *x, int64_t ldx, int M, int K, int8_t *q, float *s_a, bool pdl,
+                                cudaStream_t stream)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(M));
+    cfg.blockDim = dim3(kQuantThreads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, quantize_rows_kernel<true>, static_cast<const void *>(x), ldx, K, q, s_a,
+                              pdl ? 1 : 0);
+}
+
+cudaError_t launch_quantize_weight(const float *w, int64_t ldw, int N, int K, int8_t *w_q, float *s_w,
+                                   cudaStream_t stream)
+{
+    quantize_rows_kernel<false><<<static_cast<unsigned>(N), kQuantThreads, 0, stream>>>(w, ldw, K, w_q, s_w, 0);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_requant_pow2(const int8_t *w_q, const float *s_w, int N, int K, int8_t *w_q_out, float *s_w_out,
+                                cudaStream_t stream)
+{
+    requant_pow2_kernel<<<static_cast<unsigned>(N), kQuantThreads, 0, stream>>>(w_q, s_w, K, w_q_out, s_w_out);
+    return cudaGetLastError();
+}
+
+}  // namespace bi

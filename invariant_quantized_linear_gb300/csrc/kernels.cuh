@@ -1,0 +1,88 @@
+// Internal launch interface between the C ABI (bi_api.cu) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace bi {
+
+// ---------------------------------------------------------------- workspace
+//
+// One layout serves the skinny linear, the LM head and the prefill kernel:
+//   [0, 256)          control words: status (int), argmax ticket (int)
+//   rb_counter        kMaxGrid int32   split-K chunk counters, one per slot
+//   best              kMaxGrid * 16 uint64   per-CTA argmax keys
+//   partial           kMaxGrid * 64 * 16 int32   split-K partial sums
+// A slot is owned by the CTA in whose range a split row block starts, so at
+// most one split row block maps to a slot.  Counters and partials are reset
+// by the kernel that consumes them, so a zero-filled workspace stays zeroed.
+constexpr int kMaxGrid = 256;
+constexpr int kBM = 64;        // weight rows per row block (4 warps x 16)
+constexpr int kMaxTok = 16;    // token columns kept per partial row
+constexpr size_t kWsCtrlBytes = 256;
+constexpr size_t kWsCounterOff = kWsCtrlBytes;
+constexpr size_t kWsBestOff = kWsCounterOff + sizeof(int32_t) * kMaxGrid;
+constexpr size_t kWsPartialOff = kWsBestOff + sizeof(unsigned long long) * kMaxGrid * kMaxTok;
+constexpr size_t kWsBytes = kWsPartialOff + sizeof(int32_t) * kMaxGrid * kBM * kMaxTok;
+
+struct Workspace {
+    int *status;                 // DEV_OK / DEV_TIMEOUT
+    int *ticket;                 // CTAs finished (argmax)
+    int32_t *rb_counter;         // [kMaxGrid]
+    unsigned long long *best;    // [kMaxGrid][kMaxTok]
+    int32_t *partial;            // [kMaxGrid][kBM][kMaxTok]
+};
+
+inline Workspace workspace_view(void *ws)
+{
+    char *b = static_cast<char *>(ws);
+    Workspace w;
+    w.status = reinterpret_cast<int *>(b);
+    w.ticket = reinterpret_cast<int *>(b + 4);
+    w.rb_counter = reinterpret_cast<int32_t *>(b + kWsCounterOff);
+    w.best = reinterpret_cast<unsigned long long *>(b + kWsBestOff);
+    w.partial = reinterpret_cast<int32_t *>(b + kWsPartialOff);
+    return w;
+}
+
+// ---------------------------------------------------------------- launches
+
+cudaError_t launch_quantize_act(const uint16_t *x, int64_t ldx, int M, int K, int8_t *q, float *s_a, bool pdl,
+                                cudaStream_t stream);
+cudaError_t launch_quantize_weight(const float *w, int64_t ldw, int N, int K, int8_t *w_q, float *s_w,
+                                   cudaStream_t stream);
+cudaError_t launch_requant_pow2(const int8_t *w_q, const float *s_w, int N, int K, int8_t *w_q_out,
+                                float *s_w_out, cudaStream_t stream);
+
+struct SkinnyArgs {
+    CUtensorMap map_w;         // W [N, K] int8, box 128 B x 64 rows, 128B swizzle
+    CUtensorMap map_q;         // q [M, K] int8, box 128 B x (8 * token tiles) rows, 128B swizzle
+    const float *s_a;
+    const float *s_w;
+    uint16_t *y;               // may be null for the LM head
+    int32_t *argmax;           // null for the plain linear
+    int M, N, K;
+    Workspace ws;
+    bool pdl;
+    int grid;                  // CTAs (<= kMaxGrid)
+};
+
+// M <= 16 weight-streaming kernel (plain linear or LM head with argmax).
+cudaError_t launch_skinny(const SkinnyArgs &a, cudaStream_t stream);
+
+struct PrefillArgs {
+    CUtensorMap map_w;         // W [N, K], box 128 B x 128 rows, 128B swizzle
+    CUtensorMap map_q;         // q [M, K], box 128 B x 128 rows, 128B swizzle
+    const float *s_a;
+    const float *s_w;
+    uint16_t *y;
+    int M, N, K;
+    Workspace ws;
+    bool pdl;
+};
+
+// M > 16 tiled kernel.
+cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream);
+
+}  // namespace bi

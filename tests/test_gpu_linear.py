@@ -1,0 +1,135 @@
+"""GPU parity of bi_linear_w8a8 (weight-streaming and prefill kernels) against
+the CPU oracle, bit for bit, plus batch invariance across M."""
+import numpy as np
+import pytest
+import torch
+
+import gen
+import oracle
+from tests.gpu_util import DEV, linear, oracle_weights, quant_act, to_dev, to_np, weights
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def bi():
+    import invariant_quantized_linear_gb300 as m
+    return m
+
+
+def _case(seed, M, N, K, pow2, outliers=True):
+    x = gen.act_bf16(seed, 1, M, K, outliers=gen.outlier_channels(seed, K) if outliers else (), gain=20.0)
+    w = gen.weight_f32(seed, 0, 0, N, K)
+    return x, w
+
+
+def _check_linear(bi, x, w, pow2, flags=0):
+    q_o, s_o = oracle.quantize_act(x)
+    wq_o, sw_o = oracle_weights(oracle, w, pow2)
+    want = oracle.linear_w8a8(q_o, s_o, wq_o, sw_o)
+    q, s = quant_act(bi, x)
+    wq, sw = weights(bi, w, pow2)
+    got = to_np(linear(bi, q, s, wq, sw, flags=flags))
+    assert got.shape == want.shape
+    bad = np.argwhere(got != want)
+    assert bad.size == 0, "%d mismatches, first at %s" % (len(bad), bad[:4].tolist())
+    return got
+
+
+# shapes span several row blocks (64 rows) and units (256 bytes of K), with
+# ragged tails in N and K; M covers both token tiles of the skinny kernel and
+# the prefill kernel (M > 16)
+SKINNY = [(1, 1, 16), (2, 17, 48), (3, 100, 272), (8, 1000, 1024), (9, 1024, 1040), (16, 333, 4096),
+          (4, 4096, 4096), (5, 64, 12288), (1, 12288, 256)]
+PREFILL = [(17, 130, 256), (33, 257, 1024), (130, 300, 528), (200, 1000, 4096), (64, 64, 16)]
+
+
+@pytest.mark.parametrize("M,N,K", SKINNY + PREFILL)
+@pytest.mark.parametrize("pow2", [True, False])
+def test_linear_matches_oracle(bi, M, N, K, pow2):
+    x, w = _case(M * 7 + N, M, N, K, pow2)
+    _check_linear(bi, x, w, pow2)
+
+
+def test_linear_near_int32_bound(bi):
+    """K = 133136 (the largest multiple of 16 under the int32 bound) with
+    all-127 operands: |acc| reaches 2,147,350,544 and must not wrap."""
+    K, N = 133136, 70
+    x = np.full((2, K), 0x42FE, np.uint16)        # 127.0 in bf16 -> q = 127
+    x[1, ::2] = 0xC2FE                            # -127.0
+    w = np.full((N, K), 0.02, np.float32)
+    w[1::2, ::3] = -0.02
+    _check_linear(bi, x, w, pow2=False)
+    x3 = np.concatenate([x] * 10)[:20]            # prefill path too
+    _check_linear(bi, x3, w, pow2=False)
+
+
+@pytest.mark.parametrize("N,K", [(4096, 4096), (1024, 12288), (333, 1040)])
+def test_rows_are_batch_invariant(bi, N, K):
+    """Row r of an M-row call equals the one-row call on row r alone, for
+    M = 1..16 (both token tiles) and prefill sizes."""
+    Ms = list(range(1, 17)) + [17, 64, 130]
+    xall = gen.act_bf16(77, 1, max(Ms), K, outliers=gen.outlier_channels(77, K), gain=20.0)
+    wq, sw = weights(bi, gen.weight_f32(77, 0, 0, N, K), pow2=True)
+    single = []
+    for r in range(max(Ms)):
+        q, s = quant_act(bi, xall[r:r + 1])
+        single.append(linear(bi, q, s, wq, sw))
+    single = torch.cat(single)
+    for M in Ms:
+        q, s = quant_act(bi, xall[:M])
+        y = linear(bi, q, s, wq, sw)
+        assert torch.equal(y, single[:M]), M
+
+
+def test_pdl_flag_and_graph_capture_same_bits(bi):
+    """PDL launches, and a CUDA graph of quantise + linear with PDL, give the
+    same bits as plain launches."""
+    M, N, K = 8, 4096, 4096
+    x_np, w = _case(5, M, N, K, True)
+    wq, sw = weights(bi, w, pow2=True)
+    q, s = quant_act(bi, x_np)
+    ref = linear(bi, q, s, wq, sw)
+    ws = bi.new_workspace(M, N, K)
+    y_pdl = linear(bi, q, s, wq, sw, flags=bi.BI_FLAG_PDL, ws=ws)
+    assert torch.equal(ref, y_pdl)
+
+    x = to_dev(x_np)
+    q2 = torch.empty_like(q)
+    s2 = torch.empty_like(s)
+    y2 = torch.empty_like(ref)
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        bi.bi_quantize_act(x, q2, s2, flags=bi.BI_FLAG_PDL)      # warm-up outside capture
+        bi.bi_linear_w8a8(q2, s2, wq, sw, y2, ws, flags=bi.BI_FLAG_PDL)
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    y2.zero_()
+    with torch.cuda.graph(g, stream=stream):
+        bi.bi_quantize_act(x, q2, s2, flags=bi.BI_FLAG_PDL)
+        bi.bi_linear_w8a8(q2, s2, wq, sw, y2, ws, flags=bi.BI_FLAG_PDL)
+    for _ in range(3):
+        y2.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(y2, ref)
+
+
+def test_workspace_left_zeroed(bi):
+    M, N, K = 3, 1000, 1040   # row blocks straddle CTAs, so partial slots are used
+    x_np, w = _case(9, M, N, K, True)
+    wq, sw = weights(bi, w, pow2=True)
+    q, s = quant_act(bi, x_np)
+    ws = bi.new_workspace(M, N, K)
+    for _ in range(3):
+        linear(bi, q, s, wq, sw, ws=ws)
+        lm = torch.empty(M, dtype=torch.int32, device=DEV)
+        bi.bi_lmhead_argmax(q, s, wq, sw, None, lm, ws)
+    torch.cuda.synchronize()
+    # per-CTA argmax keys are scratch that is overwritten by every call; all
+    # counters and partial sums must be back at zero
+    from invariant_quantized_linear_gb300 import lib  # noqa: F401  (library loaded)
+    head = ws[:256 + 4 * 256]
+    part = ws[256 + 4 * 256 + 8 * 256 * 16:]
+    assert int(head.count_nonzero()) == 0 and int(part.count_nonzero()) == 0
+    assert bi.bi_workspace_status(ws) == bi.BI_OK
