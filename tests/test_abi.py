@@ -15,8 +15,8 @@ HEADER = os.path.join(ROOT, "include", "bi.h")
 
 @pytest.fixture(scope="module")
 def bi():
-    from invariant_quantized_linear_gb300 import build
-    build.build()
+    import __graft_entry__
+    __graft_entry__.build()
     import invariant_quantized_linear_gb300 as m
     return m
 
