@@ -129,15 +129,28 @@ class Stack:
         self.layers = layers
         wl = gen.STACK36
         self.lin = gen.QWEN3_8B_LINEARS
-        self.W = []       # per layer: dict name -> (wq, sw)
+        # Per layer, q/k/v share one input and so do gate/up: their weight
+        # rows are stored back to back ("packed") and each group is one call.
+        # Rows are independent, so the outputs are the same bits as separate
+        # calls.
+        self.groups = [("qkv", ("q", "k", "v"), 4096), ("o", ("o",), 4096), ("gu", ("gate", "up"), 4096),
+                       ("down", ("down",), 12288)]
+        byname = {l.name: l for l in self.lin}
+        self.W = []       # per layer: dict group -> (wq, sw) with the group's rows packed
         self.chunk = 8192
         self.stage = torch.empty(self.chunk * 12288, dtype=torch.float32).pin_memory()
         stage_np = self.stage.numpy()
         for l in range(layers):
             d = {}
-            for lin in self.lin:
-                d[lin.name] = self._make_weight(lambda r0, r, lin=lin, l=l: gen.weight_f32(
-                    wl.seed, l, lin.proj, lin.N, lin.K, row0=r0, rows=r, out=stage_np), lin.N, lin.K)
+            for gname, members, K in self.groups:
+                parts = [self._make_weight(lambda r0, r, lin=byname[m], l=l: gen.weight_f32(
+                    wl.seed, l, lin.proj, lin.N, lin.K, row0=r0, rows=r, out=stage_np), byname[m].N, K)
+                    for m in members]
+                if len(parts) == 1:
+                    d[gname] = parts[0]
+                else:
+                    d[gname] = (torch.cat([p[0] for p in parts]), torch.cat([p[1] for p in parts]))
+                    del parts
             self.W.append(d)
         # LM head with the planted near-tie rows for the head's activation rows
         self.x_head_np = gen.activations(wl, 16, gen.LMHEAD.K, stream=7)
@@ -148,7 +161,7 @@ class Stack:
         self.weight_bytes = sum(l.N * l.K + 4 * l.N for l in self.lin) * layers + \
             gen.LMHEAD.N * gen.LMHEAD.K + 4 * gen.LMHEAD.N
         # activations: inputs of q/k/v, o, gate/up, down per layer, and the head
-        self.in_dims = [("qkv", 4096), ("o", 4096), ("gu", 4096), ("down", 12288)]
+        self.in_dims = [(g, K) for g, _, K in self.groups]
         self.x_np = {}
         self.x = {}
         for l in range(layers):
@@ -161,7 +174,8 @@ class Stack:
         self.ws = bi.new_workspace(16, 151936, 12288, device=device)
         self.q = torch.empty((16, 12288), dtype=torch.int8, device=device)
         self.s = torch.empty(16, dtype=torch.float32, device=device)
-        self.y = {lin.name: torch.empty((16, lin.N), dtype=torch.int16, device=device) for lin in self.lin}
+        self.y = {g: torch.empty((16, self.W[0][g][0].shape[0]), dtype=torch.int16, device=device)
+                  for g, _, _ in self.groups}
         self.argmax = torch.empty(16, dtype=torch.int32, device=device)
         torch.cuda.synchronize()
 
@@ -179,24 +193,30 @@ class Stack:
         return wq, sw
 
     def launches_per_step(self):
-        return self.layers * (len(self.in_dims) + len(self.lin)) + 2
+        return self.layers * 2 * len(self.groups) + 2
 
-    def step(self, M, flags, timer=None):
-        """Enqueue one verify pass on the current stream.  timer(name, bytes)
-        returns a context that brackets one linear launch with events."""
+    def linear_bytes(self, M):
+        """Algorithmic bytes of the step's linear launches: W + s_w + q + s_a + y."""
+        tot = 0
+        for l in range(self.layers):
+            for nm, K in self.in_dims:
+                N = self.W[l][nm][0].shape[0]
+                tot += N * K + 4 * N + M * K + 4 * M + 2 * M * N
+        return tot
+
+    def step(self, M, flags, linears_only=False):
+        """Enqueue one verify pass on the current stream (or, with
+        linears_only, just its linear launches back to back)."""
         bi, q, s = self.bi, self.q[:M], self.s[:M]
-        groups = {"qkv": ("q", "k", "v"), "o": ("o",), "gu": ("gate", "up"), "down": ("down",)}
         for l in range(self.layers):
             for nm, K in self.in_dims:
                 qbuf = self.q.view(-1)[:M * K].view(M, K)
-                bi.bi_quantize_act(self.x[(l, nm)][:M, :K], qbuf, s, K=K, flags=flags)
-                for pn in groups[nm]:
-                    wq, sw = self.W[l][pn]
-                    if timer is None:
-                        bi.bi_linear_w8a8(qbuf, s, wq, sw, self.y[pn][:M], self.ws, flags=flags)
-                    else:
-                        with timer(wq.shape[0] * K + 4 * wq.shape[0] + M * K + 4 * M + 2 * M * wq.shape[0]):
-                            bi.bi_linear_w8a8(qbuf, s, wq, sw, self.y[pn][:M], self.ws, flags=flags)
+                if not linears_only:
+                    bi.bi_quantize_act(self.x[(l, nm)][:M, :K], qbuf, s, K=K, flags=flags)
+                wq, sw = self.W[l][nm]
+                bi.bi_linear_w8a8(qbuf, s, wq, sw, self.y[nm][:M], self.ws, flags=flags)
+        if linears_only:
+            return
         K = 4096
         qbuf = self.q.view(-1)[:M * K].view(M, K)
         bi.bi_quantize_act(self.x[("head",)][:M], qbuf, s, K=K, flags=flags)
@@ -277,32 +297,18 @@ def run_ours(args):
                              "weight_gbs": round(st.weight_bytes / (msm * 1e-3) / 1e9, 1),
                              "tokens_per_s_eq": round(m / (msm * 1e-3), 1)}
 
-    # dominant kernel: each weight-streaming launch of one pass bracketed by
-    # events on its stream (plain launches, no graph, no PDL)
-    durations, byts = [], []
-
-    class Timer:
-        def __init__(self, nbytes):
-            self.nbytes = nbytes
-
-        def __enter__(self):
-            self.a = torch.cuda.Event(enable_timing=True)
-            self.b = torch.cuda.Event(enable_timing=True)
-            self.a.record(stream)
-
-        def __exit__(self, *exc):
-            self.b.record(stream)
-            durations.append((self.a, self.b))
-            byts.append(self.nbytes)
-
+    # dominant kernel: the step's weight-streaming linear launches alone,
+    # back to back in a CUDA graph (same launch configuration as the step),
+    # timed with events on the launching stream
     with torch.cuda.stream(stream):
-        st.step(M, 0)
-        durations.clear()
-        byts.clear()
-        st.step(M, 0, timer=Timer)
+        st.step(M, flags, linears_only=True)
     stream.synchronize()
-    tot_ms = sum(a.elapsed_time(b) for a, b in durations)
-    achieved = sum(byts) / (tot_ms * 1e-3) / 1e9
+    gl = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gl, stream=stream):
+        st.step(M, flags, linears_only=True)
+    lin_launches = st.layers * len(st.groups)
+    lin_ms = time_graph(gl, max(5, args.steps // 2), 3)
+    achieved = st.linear_bytes(M) / (lin_ms * 1e-3) / 1e9
 
     # end to end: activations H2D from pinned memory, graph, argmax D2H
     host_x = {k: torch.from_numpy(v.view(np.int16)).pin_memory() for k, v in st.x_np.items()}
@@ -342,7 +348,8 @@ def run_ours(args):
             "config": {"workload": WORKLOAD, "M": M, "layers": args.layers, "hidden": 4096,
                        "intermediate": 12288, "vocab": 151936, "weight_bytes_per_step": st.weight_bytes,
                        "l2": "inputs larger than L2 (all weights read once per step)",
-                       "activations": "independent synthetic input per linear (layers not chained)",
+                       "activations": "independent synthetic input per linear group (layers not chained)",
+                       "packing": "q/k/v and gate/up weight rows packed: one call per group",
                        "launch": "CUDA graph of the step, programmatic dependent launch",
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "pct_of_hbm_copy": round(100 * gbs / world / peak, 1),
@@ -351,9 +358,10 @@ def run_ours(args):
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": traffic,
                          "kernel": "skinny_kernel (bi_linear_w8a8, M<=16)",
+                         "launch_us": round(lin_ms * 1e3 / lin_launches, 3),
                          "peak_kind": kind, "note": "achieved = algorithmic bytes (W + s_w + q + s_a + y) "
-                                                   "per launch / event-timed launch duration, summed over "
-                                                   "the 252 linear launches of one pass"},
+                                                   "of the step's %d linear launches / their event-timed "
+                                                   "duration back to back in a CUDA graph" % lin_launches},
             "e2e": {"value": round(e2e_gbs, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": 4 * M, "ms_per_step": round(e2e_ms, 4)},
             "gpu_launches": st.launches_per_step() * args.steps,

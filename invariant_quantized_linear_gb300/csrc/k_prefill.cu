@@ -2,10 +2,13 @@
 // contraction with exact int32 accumulation and the same per-element
 // epilogue as the weight-streaming kernel, so every row matches it bitwise.
 //
-// sm_103a has no int8 kind for tcgen05.mma, so the contraction runs on the
-// int8 warp-level tensor-core MMA (m16n8k32, int32 accumulate).  Tiles are
-// moved by TMA into a ring of 128-byte-swizzled shared-memory stages by one
-// producer warp; eight consumer warps each own a 32-token x 64-row tile.
+// sm_103a has no int8 kind for tcgen05.mma, and its warp-level int8 MMA runs
+// at a fraction of the f16 rate, so the contraction runs on f16 tensor-core
+// MMAs (m16n8k16, fp32 accumulate) over int8 values converted exactly to f16;
+// fp32 partials are moved into int32 totals while they are integers far below
+// 2^24, so the sum is the exact integer dot product.  Tiles are moved by TMA
+// into a ring of 128-byte-swizzled shared-memory stages by one producer warp;
+// eight consumer warps each own a 32-token x 64-row tile.
 // CTA tile: 128 tokens x 128 weight rows, 128 bytes of K per stage.
 #include "kernels.cuh"
 #include "ptx.cuh"
@@ -100,11 +103,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t b_row = wn * 64 + ((mat & 2) ? 8 : 0) + r8;
     const int b_hi = mat & 1;
 
+    // int32 totals; fp32 tensor-core partials are moved into them every two
+    // stages (256 bytes of K: |partial| <= 256 * 127^2 < 2^22, exact in fp32)
     int32_t acc[2][8][4];
+    float facc[2][8][4];
 #pragma unroll
     for (int i = 0; i < 2; ++i)
 #pragma unroll
-        for (int jn = 0; jn < 8; ++jn) acc[i][jn][0] = acc[i][jn][1] = acc[i][jn][2] = acc[i][jn][3] = 0;
+        for (int jn = 0; jn < 8; ++jn)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                acc[i][jn][e] = 0;
+                facc[i][jn][e] = 0.0f;
+            }
 
     for (int j = 0; j < p.kt; ++j) {
         const int s = j % kStages;
@@ -119,23 +130,49 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t wb = smem_u32(sW + s * kStageW);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
-            uint32_t a[2][4];
+            // int8 fragments of 32 bytes of K (chunks X and Y)
+            uint32_t a8[2][4];
 #pragma unroll
             for (int i = 0; i < 2; ++i)
-                ldmatrix_x4(qb + swz128(a_tok + 16 * i, 2 * ks + a_hi), a[i][0], a[i][1], a[i][2], a[i][3]);
+                ldmatrix_x4(qb + swz128(a_tok + 16 * i, 2 * ks + a_hi), a8[i][0], a8[i][1], a8[i][2], a8[i][3]);
+            uint32_t b8[4][4];
 #pragma unroll
-            for (int jp = 0; jp < 4; ++jp) {
-                uint32_t b0, b1, b2, b3;
-                ldmatrix_x4(wb + swz128(b_row + 16 * jp, 2 * ks + b_hi), b0, b1, b2, b3);
+            for (int jp = 0; jp < 4; ++jp)
+                ldmatrix_x4(wb + swz128(b_row + 16 * jp, 2 * ks + b_hi), b8[jp][0], b8[jp][1], b8[jp][2], b8[jp][3]);
+#pragma unroll
+            for (int xy = 0; xy < 2; ++xy) {
+                uint32_t a[2][4];
 #pragma unroll
                 for (int i = 0; i < 2; ++i) {
-                    mma_s8_16832(acc[i][2 * jp], a[i][0], a[i][1], a[i][2], a[i][3], b0, b1);
-                    mma_s8_16832(acc[i][2 * jp + 1], a[i][0], a[i][1], a[i][2], a[i][3], b2, b3);
+                    i8x4_to_f16x2x2(a8[i][2 * xy], a[i][0], a[i][2]);      // token g
+                    i8x4_to_f16x2x2(a8[i][2 * xy + 1], a[i][1], a[i][3]);  // token g + 8
+                }
+#pragma unroll
+                for (int jp = 0; jp < 4; ++jp) {
+                    uint32_t b0, b1, b2, b3;
+                    i8x4_to_f16x2x2(b8[jp][xy], b0, b1);       // rows 0-7 of the pair
+                    i8x4_to_f16x2x2(b8[jp][2 + xy], b2, b3);   // rows 8-15
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) {
+                        mma_f16_16816(facc[i][2 * jp], a[i][0], a[i][1], a[i][2], a[i][3], b0, b1);
+                        mma_f16_16816(facc[i][2 * jp + 1], a[i][0], a[i][1], a[i][2], a[i][3], b2, b3);
+                    }
                 }
             }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
+        if ((j & 1) || j + 1 == p.kt) {
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+#pragma unroll
+                for (int jn = 0; jn < 8; ++jn)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        acc[i][jn][e] += f2i_exact(facc[i][jn][e]);
+                        facc[i][jn][e] = 0.0f;
+                    }
+        }
     }
     if (*abort_flag) return;
 

@@ -16,6 +16,7 @@ namespace {
 
 constexpr int kQuantThreads = 256;
 
+template <int THREADS = kQuantThreads>
 __device__ __forceinline__ float block_max(float v, float *red)
 {
 #pragma unroll
@@ -24,7 +25,7 @@ __device__ __forceinline__ float block_max(float v, float *red)
     if (lane == 0) red[warp] = v;
     __syncthreads();
     if (warp == 0) {
-        v = (lane < kQuantThreads / 32) ? red[lane] : 0.0f;
+        v = (lane < THREADS / 32) ? red[lane] : 0.0f;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
         if (lane == 0) red[0] = v;
@@ -89,7 +90,7 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_rows_kernel(const void
 #pragma unroll
         for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
     }
-    amax = block_max(amax, red);
+    amax = block_max<kQuantThreads>(amax, red);
     const float s = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 127.0f);
 
     int8_t *qr = q + row * K;
@@ -106,6 +107,58 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_rows_kernel(const void
             w[i] = b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
         }
         *reinterpret_cast<uint4 *>(qr + k) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    if (threadIdx.x == 0) s_out[row] = s;
+}
+
+// Activation rows up to 16384 elements: one CTA of 256 threads per row, each
+// thread holding C chunks of 8 bf16 values in registers, so the row is read
+// from memory once and the kernel is one load, one block reduction and one
+// store deep.  The CTA is small so that it fits beside a running linear-layer
+// CTA when launched as a programmatic dependent.
+constexpr int kActThreads = 256;
+
+template <int C>
+__global__ void __launch_bounds__(kActThreads) quantize_act_reg_kernel(const uint16_t *__restrict__ x, int64_t ldx,
+                                                                       int K, int8_t *__restrict__ q,
+                                                                       float *__restrict__ s_out, int pdl)
+{
+    __shared__ float red[kActThreads / 32];
+    if (pdl) {
+        pdl_launch_dependents();
+        pdl_wait();
+    }
+    const int64_t row = blockIdx.x;
+    const uint16_t *xr = x + row * ldx;
+    uint4 v[C];
+    float amax = 0.0f;
+#pragma unroll
+    for (int c = 0; c < C; ++c) {
+        const int k = (c * kActThreads + threadIdx.x) * 8;
+        v[c] = (k < K) ? *reinterpret_cast<const uint4 *>(xr + k) : make_uint4(0, 0, 0, 0);
+        const uint32_t w[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            amax = fmaxf(amax, fabsf(__uint_as_float(w[i] << 16)));
+            amax = fmaxf(amax, fabsf(__uint_as_float(w[i] & 0xFFFF0000u)));
+        }
+    }
+    amax = block_max<kActThreads>(amax, red);
+    const float s = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 127.0f);
+    int8_t *qr = q + row * K;
+#pragma unroll
+    for (int c = 0; c < C; ++c) {
+        const int k = (c * kActThreads + threadIdx.x) * 8;
+        if (k >= K) continue;
+        const uint32_t w[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
+        uint32_t o[2] = {0, 0};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t lo = static_cast<uint8_t>(quant1(__uint_as_float(w[i] << 16), s));
+            const uint32_t hi = static_cast<uint8_t>(quant1(__uint_as_float(w[i] & 0xFFFF0000u), s));
+            o[i >> 1] |= (lo | (hi << 8)) << (16 * (i & 1));
+        }
+        *reinterpret_cast<uint2 *>(qr + k) = make_uint2(o[0], o[1]);
     }
     if (threadIdx.x == 0) s_out[row] = s;
 }
@@ -191,15 +244,28 @@ cudaError_t launch_quantize_act(const uint16_t *x, int64_t ldx, int M, int K, in
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(M));
-    cfg.blockDim = dim3(kQuantThreads);
+    cfg.blockDim = dim3(kActThreads);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, quantize_rows_kernel<true>, static_cast<const void *>(x), ldx, K, q, s_a,
-                              pdl ? 1 : 0);
+    const int p = pdl ? 1 : 0;
+    const int chunks = (K + kActThreads * 8 - 1) / (kActThreads * 8);
+    switch (chunks) {
+    case 1: return cudaLaunchKernelEx(&cfg, quantize_act_reg_kernel<1>, x, ldx, K, q, s_a, p);
+    case 2: return cudaLaunchKernelEx(&cfg, quantize_act_reg_kernel<2>, x, ldx, K, q, s_a, p);
+    case 3: return cudaLaunchKernelEx(&cfg, quantize_act_reg_kernel<3>, x, ldx, K, q, s_a, p);
+    case 4: return cudaLaunchKernelEx(&cfg, quantize_act_reg_kernel<4>, x, ldx, K, q, s_a, p);
+    case 5: return cudaLaunchKernelEx(&cfg, quantize_act_reg_kernel<5>, x, ldx, K, q, s_a, p);
+    case 6: return cudaLaunchKernelEx(&cfg, quantize_act_reg_kernel<6>, x, ldx, K, q, s_a, p);
+    case 7: return cudaLaunchKernelEx(&cfg, quantize_act_reg_kernel<7>, x, ldx, K, q, s_a, p);
+    case 8: return cudaLaunchKernelEx(&cfg, quantize_act_reg_kernel<8>, x, ldx, K, q, s_a, p);
+    default: break;
+    }
+    cfg.blockDim = dim3(kQuantThreads);
+    return cudaLaunchKernelEx(&cfg, quantize_rows_kernel<true>, static_cast<const void *>(x), ldx, K, q, s_a, p);
 }
 
 cudaError_t launch_quantize_weight(const float *w, int64_t ldw, int N, int K, int8_t *w_q, float *s_w,

@@ -10,9 +10,15 @@
 //  * a producer warp moves each unit's weight tile and the matching slice of
 //    the int8 activations into a ring of shared-memory stages with TMA
 //    (128-byte swizzle, evict-first L2 policy for the weights);
-//  * four consumer warps own 16 weight rows each and run int8 tensor-core
-//    MMAs (m16n8k32: weight rows as the 16-row operand, tokens as the 8
-//    columns) into int32 accumulators;
+//  * eight consumer warps: four 16-row groups, each row group's 256 bytes
+//    of K per stage split between two warps.  Half of the 32-byte K groups
+//    (a quarter with 9..16 tokens) run on the int8 tensor-core MMA
+//    (m16n8k32, int32 accumulate); the rest are converted exactly to f16 and
+//    run on the f16 MMA (m16n8k16, fp32 accumulate), whose partials (integers
+//    below 2^20) are moved into the int32 accumulators every stage.  On
+//    sm_103a the int8 MMA alone runs at a fraction of the f16 rate and the
+//    f16 MMA alone costs an int8 -> f16 conversion per operand; the split
+//    keeps both pipes and the ALU clear of the weight stream's pace;
 //  * a row block whose K range straddles two CTAs is finished through int32
 //    atomics in the workspace; the CTA that completes the count applies the
 //    epilogue.  Integer sums are exact, so the split, the MMA order and the
@@ -30,7 +36,9 @@ namespace bi {
 
 namespace {
 
-constexpr int kConsumerWarps = 4;
+constexpr int kRowGroups = 4;                       // 16-row groups per 64-row block
+constexpr int kKSplit = 2;                          // warps sharing one row group's K
+constexpr int kConsumerWarps = kRowGroups * kKSplit;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kNch = 2;                    // 128-byte chunks of K per unit
 constexpr int kUnitK = kNch * 128;         // bytes of K per unit
@@ -42,8 +50,10 @@ struct Cfg {
     static constexpr int kAChunkBytes = kTok * 128;             // 1 or 2 KB
     static constexpr int kWStage = kNch * kWChunkBytes;         // 16 KB
     static constexpr int kAStage = kNch * kAChunkBytes;         // 2 or 4 KB
-    static constexpr int kStages = (MT == 1) ? 6 : 5;           // <= ~110 KB of shared memory
-    static constexpr int kSmemBytes = kStages * (kWStage + kAStage) + 1024 /*align*/ + 1024 /*barriers, flags*/;
+    static constexpr int kStages = (MT == 1) ? 5 : 4;           // two CTAs per SM fit
+    static constexpr int kRedBytes = (kKSplit - 1) * kBM * kMaxTok * 4;  // cross-warp K reduction
+    static constexpr int kCtlBytes = 2 * kStages * 8 + 16 + kConsumerWarps * kMaxTok * 8;  // barriers, flags, keys
+    static constexpr int kSmemBytes = kStages * (kWStage + kAStage) + kRedBytes + 1024 /*align*/ + kCtlBytes;
 };
 
 struct Params {
@@ -69,6 +79,17 @@ __device__ __forceinline__ int unit_owner(long long u, long long units, int G)
     return static_cast<int>(((u + 1) * G - 1) / units);
 }
 
+// Which 32-byte groups of K run on the int8 MMA (no conversion; a separate,
+// slower pipe) and which on the f16 MMA (fast, but each int8 operand is first
+// converted): splitting the groups keeps both pipes and the ALU below their
+// limits at HBM speed.  With two token tiles the int8 MMA does twice the work
+// per group, so it takes a smaller share.
+template <int MT>
+__device__ __forceinline__ constexpr bool imma_group(int t)
+{
+    return MT == 1 ? (t & 1) == 0 : (t & 3) == 0;
+}
+
 __device__ __forceinline__ void consumer_bar()
 {
     asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
@@ -85,7 +106,7 @@ __device__ __forceinline__ unsigned long long argmax_key(uint16_t b, int n)
 }
 
 template <int MT, bool ARGMAX>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
     skinny_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_q, Params p)
 {
     using C = Cfg<MT>;
@@ -93,11 +114,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sW = smem;                                   // [stages][kNch][64 rows][128 B]
     uint8_t *sA = smem + C::kStages * C::kWStage;         // [stages][kNch][kTok rows][128 B]
-    uint64_t *full = reinterpret_cast<uint64_t *>(sA + C::kStages * C::kAStage);
+    int32_t *sred = reinterpret_cast<int32_t *>(sA + C::kStages * C::kAStage);   // [kKSplit-1][64][16]
+    uint64_t *full = reinterpret_cast<uint64_t *>(sA + C::kStages * C::kAStage + C::kRedBytes);
     uint64_t *empty = full + C::kStages;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + C::kStages);
-    volatile int *last_flag = abort_flag + 1;
-    unsigned long long *sbest = reinterpret_cast<unsigned long long *>(empty + C::kStages + 2);  // [4][16]
+    volatile int *last_flag = abort_flag + 1;  // [2]
+    unsigned long long *sbest = reinterpret_cast<unsigned long long *>(empty + C::kStages + 2);  // [warps][16]
+    static_assert(sizeof(uint64_t) * 2 >= 3 * sizeof(int), "flags fit before sbest");
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = gridDim.x;
@@ -105,14 +128,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     const long long u_end = range_start(blockIdx.x + 1, p.units, G);
     const int n_units = static_cast<int>(u_end - u_begin);
 
-    if (threadIdx.x == 0) {
+    // The producer thread sets up the barriers and starts the first weight
+    // copies before the CTA-wide barrier, so DRAM is busy as early as possible.
+    const bool producer = (threadIdx.x == kConsumerWarps * 32);
+    const uint32_t stage_bytes = C::kWStage + C::kAStage;
+    const int n_pre = n_units < C::kStages ? n_units : C::kStages;
+    uint64_t pol_w = 0, pol_a = 0;
+    int w_rb = 0, w_c = 0, a_c = 0;   // next weight / activation unit to issue
+    if (producer) {
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kConsumerWarps);
         }
         *abort_flag = 0;
-        *last_flag = 0;
+        last_flag[0] = last_flag[1] = 0;
         fence_mbarrier_init();
+        if (n_units > 0) {
+            pol_w = policy_evict_first();
+            pol_a = policy_evict_last();
+            // unit j of this CTA is (row block, K unit) = (rb0, c0) advanced j
+            // times along K, wrapping to the next row block
+            w_rb = static_cast<int>(u_begin / p.upr);
+            w_c = static_cast<int>(u_begin % p.upr);
+            a_c = w_c;
+            for (int j = 0; j < n_pre; ++j) {
+                mbar_arrive_expect_tx(&full[j], stage_bytes);
+#pragma unroll
+                for (int ch = 0; ch < kNch; ++ch)
+                    tma_load_2d(sW + j * C::kWStage + ch * kWChunkBytes, &map_w, &full[j], w_c * kUnitK + ch * 128,
+                                w_rb * kBM, pol_w);
+                if (++w_c == p.upr) {
+                    w_c = 0;
+                    ++w_rb;
+                }
+            }
+        }
     }
     __syncthreads();
     if (p.pdl) pdl_launch_dependents();
@@ -120,36 +170,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kConsumerWarps) {
         // ------------------------------------------------------------ producer
         if (lane == 0 && n_units > 0) {
-            prefetch_tensormap(&map_w);
-            prefetch_tensormap(&map_q);
-            const uint64_t pol_w = policy_evict_first();
-            const uint64_t pol_a = policy_evict_last();
-            const uint32_t stage_bytes = C::kWStage + C::kAStage;
             auto issue_w = [&](int j) {
                 const int s = j % C::kStages;
-                const long long u = u_begin + j;
-                const int rb = static_cast<int>(u / p.upr), c = static_cast<int>(u % p.upr);
 #pragma unroll
                 for (int ch = 0; ch < kNch; ++ch)
-                    tma_load_2d(sW + s * C::kWStage + ch * kWChunkBytes, &map_w, &full[s], c * kUnitK + ch * 128,
-                                rb * kBM, pol_w);
+                    tma_load_2d(sW + s * C::kWStage + ch * kWChunkBytes, &map_w, &full[s], w_c * kUnitK + ch * 128,
+                                w_rb * kBM, pol_w);
+                if (++w_c == p.upr) {
+                    w_c = 0;
+                    ++w_rb;
+                }
             };
             auto issue_a = [&](int j) {
                 const int s = j % C::kStages;
-                const long long u = u_begin + j;
-                const int c = static_cast<int>(u % p.upr);
 #pragma unroll
                 for (int ch = 0; ch < kNch; ++ch)
-                    tma_load_2d(sA + s * C::kAStage + ch * C::kAChunkBytes, &map_q, &full[s], c * kUnitK + ch * 128,
+                    tma_load_2d(sA + s * C::kAStage + ch * C::kAChunkBytes, &map_q, &full[s], a_c * kUnitK + ch * 128,
                                 0, pol_a);
+                if (++a_c == p.upr) a_c = 0;
             };
-            // The weights do not depend on the preceding kernel: start them
-            // before waiting for it; the activations only after.
-            const int n_pre = n_units < C::kStages ? n_units : C::kStages;
-            for (int j = 0; j < n_pre; ++j) {
-                mbar_arrive_expect_tx(&full[j], stage_bytes);
-                issue_w(j);
-            }
+            // The weights do not depend on the preceding kernel and were
+            // started above; the activations only after waiting for it.
             if (p.pdl) pdl_wait();
             for (int j = 0; j < n_pre; ++j) issue_a(j);
             int issued = n_pre;
@@ -181,7 +222,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int g = lane >> 2, tq = lane & 3;
     const int mat = lane >> 3, r8 = lane & 7;
     // ldmatrix row addresses: weight rows for the A operand, token rows for B
-    const uint32_t a_row = warp * 16 + ((mat & 1) ? 8 : 0) + r8;
+    const int rg = warp % kRowGroups;   // 16-row group inside the row block
+    const int kq = warp / kRowGroups;   // which share of each stage's K this warp takes
+    const uint32_t a_row = rg * 16 + ((mat & 1) ? 8 : 0) + r8;
     const int a_hi = (mat & 2) ? 1 : 0;                    // chunk X or Y
     const uint32_t b_tok = (MT == 2 && (lane >> 4)) ? 8 + r8 : r8;
     const int b_hi = (lane >> 3) & 1;
@@ -190,6 +233,52 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int t = 0; t < MT; ++t) best[t][0] = best[t][1] = 0ull;
 
+    // activation scales of the tokens this thread's accumulators hold
+    float sa_reg[MT][2];
+#pragma unroll
+    for (int t = 0; t < MT; ++t)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int tok = 8 * t + 2 * tq + e;
+            sa_reg[t][e] = tok < p.M ? p.s_a[tok] : 0.0f;
+        }
+    // weight scales of rows g and g + 8 of this warp's row group
+    auto load_sw = [&](int rb, float (&sw)[2]) {
+        const int n0 = rb * kBM + rg * 16 + g;
+        sw[0] = n0 < p.N ? p.s_w[n0] : 0.0f;
+        sw[1] = n0 + 8 < p.N ? p.s_w[n0 + 8] : 0.0f;
+    };
+
+    // Epilogue of one finished 16-row x (8 * MT)-token tile of this warp.
+    auto epilogue = [&](int rb, const int32_t (&v)[MT][4], const float (&sw)[2]) {
+        const int n0 = rb * kBM + rg * 16 + g;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int n = n0 + ((i & 2) ? 8 : 0);
+            if (n >= p.N) continue;
+#pragma unroll
+            for (int t = 0; t < MT; ++t) {
+                const int tok = 8 * t + 2 * tq + (i & 1);
+                if (tok >= p.M) continue;
+                float f = __int2float_rn(v[t][i]);
+                f = __fmul_rn(f, sa_reg[t][i & 1]);
+                f = __fmul_rn(f, sw[(i & 2) ? 1 : 0]);
+                const uint16_t b = __bfloat16_as_ushort(__float2bfloat16_rn(f));
+                if (p.y) p.y[static_cast<size_t>(tok) * p.N + n] = b;
+                if constexpr (ARGMAX) {
+                    const unsigned long long key = argmax_key(b, n);
+                    if (key > best[t][i & 1]) best[t][i & 1] = key;
+                }
+            }
+        }
+    };
+
+    // Row blocks this CTA covers only in part: their partial sums go to the
+    // workspace now (fire-and-forget atomics) and are settled after the loop,
+    // so the stream of weights never waits on a global round trip.
+    int pend_rb[2] = {0, 0}, pend_n[2] = {0, 0};
+    int npend = 0;
+
     int j = 0;
     long long u = u_begin;
     while (u < u_end) {
@@ -197,9 +286,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int c0 = static_cast<int>(u % p.upr);
         const long long left = u_end - u;
         const int nch = (p.upr - c0) < left ? (p.upr - c0) : static_cast<int>(left);
-        int32_t acc[MT][4];
+        int32_t v[MT][4];
 #pragma unroll
-        for (int t = 0; t < MT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0;
+        for (int t = 0; t < MT; ++t) v[t][0] = v[t][1] = v[t][2] = v[t][3] = 0;
+        float sw[2];
+        load_sw(rb, sw);   // in flight while the row block's stages stream
 
         for (int it = 0; it < nch; ++it, ++j) {
             const int s = j % C::kStages;
@@ -212,93 +303,146 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const uint32_t wbase = smem_u32(sW + s * C::kWStage);
             const uint32_t abase = smem_u32(sA + s * C::kAStage);
+            // All int8 fragments of the stage first (the loads overlap), then
+            // exact int8 -> f16 conversion and f16 tensor-core MMAs into two
+            // fp32 accumulators.  One ldmatrix group covers 32 bytes of K:
+            // A regs r0/r1 = rows g / g+8 of 16-byte chunk X, r2/r3 = chunk Y;
+            // B regs = token rows of chunks X and Y.  Logical k of the MMA is
+            // a fixed permutation of the bytes, identical for A and B, so the
+            // integer dot product is unchanged.
+            constexpr int kGroups = kNch * 4 / kKSplit;   // 32-byte groups of K per warp per stage
+            uint32_t fa[kGroups][4];
+            uint32_t fb[kGroups][2 * MT];
 #pragma unroll
-            for (int ch = 0; ch < kNch; ++ch) {
+            for (int tt = 0; tt < kGroups; ++tt) {
+                const int t = kq * kGroups + tt;
+                const int ch = t >> 2, ks = t & 3;
+                ldmatrix_x4(wbase + ch * kWChunkBytes + swz128(a_row, 2 * ks + a_hi), fa[tt][0], fa[tt][1],
+                            fa[tt][2], fa[tt][3]);
+                if constexpr (MT == 1)
+                    ldmatrix_x2(abase + ch * C::kAChunkBytes + swz128(b_tok, 2 * ks + b_hi), fb[tt][0], fb[tt][1]);
+                else
+                    ldmatrix_x4(abase + ch * C::kAChunkBytes + swz128(b_tok, 2 * ks + b_hi), fb[tt][0], fb[tt][1],
+                                fb[tt][2], fb[tt][3]);
+            }
+            float facc[2][MT][4];
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks) {
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int m = 0; m < MT; ++m) facc[h][m][0] = facc[h][m][1] = facc[h][m][2] = facc[h][m][3] = 0.0f;
+#pragma unroll
+            for (int t = 0; t < kGroups; ++t) {
+                if (imma_group<MT>(t)) {
+                    // int8 tensor-core MMA on the raw codes, straight into int32
+#pragma unroll
+                    for (int m = 0; m < MT; ++m)
+                        mma_s8_16832(v[m], fa[t][0], fa[t][1], fa[t][2], fa[t][3], fb[t][2 * m], fb[t][2 * m + 1]);
+                    continue;
+                }
+#pragma unroll
+                for (int xy = 0; xy < 2; ++xy) {   // chunk X, then chunk Y
                     uint32_t a0, a1, a2, a3;
-                    ldmatrix_x4(wbase + ch * kWChunkBytes + swz128(a_row, 2 * ks + a_hi), a0, a1, a2, a3);
-                    if constexpr (MT == 1) {
+                    i8x4_to_f16x2x2(fa[t][2 * xy], a0, a2);      // row g
+                    i8x4_to_f16x2x2(fa[t][2 * xy + 1], a1, a3);  // row g + 8
+#pragma unroll
+                    for (int m = 0; m < MT; ++m) {
                         uint32_t b0, b1;
-                        ldmatrix_x2(abase + ch * C::kAChunkBytes + swz128(b_tok, 2 * ks + b_hi), b0, b1);
-                        mma_s8_16832(acc[0], a0, a1, a2, a3, b0, b1);
-                    } else {
-                        uint32_t b0, b1, b2, b3;
-                        ldmatrix_x4(abase + ch * C::kAChunkBytes + swz128(b_tok, 2 * ks + b_hi), b0, b1, b2, b3);
-                        mma_s8_16832(acc[0], a0, a1, a2, a3, b0, b1);
-                        mma_s8_16832(acc[1], a0, a1, a2, a3, b2, b3);
+                        i8x4_to_f16x2x2(fb[t][2 * m + xy], b0, b1);
+                        mma_f16_16816(facc[xy][m], a0, a1, a2, a3, b0, b1);
                     }
                 }
             }
+            // every fragment has been consumed by an issued MMA, so the
+            // stage's shared memory has been read: hand it back
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
+            // per stage each fp32 partial covers at most 64 bytes of K: an
+            // integer of magnitude <= 64 * 127^2 < 2^20, moved exactly into int32
+#pragma unroll
+            for (int m = 0; m < MT; ++m)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) v[m][i] += f2i_exact(facc[0][m][i]) + f2i_exact(facc[1][m][i]);
         }
 
-        // ---------------------------------------------------- row-block flush
-        bool finish = (c0 == 0 && nch == p.upr);
-        if (!finish) {
-            const int slot = unit_owner(static_cast<long long>(rb) * p.upr, p.units, G);
-            int32_t *part = p.ws.partial + static_cast<size_t>(slot) * (kBM * kMaxTok);
-            if (!*abort_flag) {
+        // the kKSplit warps of a row group hold partial sums of the same
+        // outputs: fold them into the kq == 0 warp through shared memory
+        if constexpr (kKSplit > 1) {
+            if (kq > 0) {
 #pragma unroll
                 for (int t = 0; t < MT; ++t)
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int r = warp * 16 + g + ((i & 2) ? 8 : 0);
-                        const int tok = 8 * t + 2 * tq + (i & 1);
-                        if (acc[t][i] != 0) atomicAdd(&part[r * kMaxTok + tok], acc[t][i]);
-                    }
-                __threadfence();
+                    for (int i = 0; i < 4; ++i)
+                        sred[((kq - 1) * kBM + rg * 16 + g + ((i & 2) ? 8 : 0)) * kMaxTok + 8 * t + 2 * tq + (i & 1)] =
+                            v[t][i];
             }
             consumer_bar();
-            if (threadIdx.x == 0) {
-                int last = 0;
-                if (!*abort_flag) {
-                    __threadfence();
-                    const int old = atomicAdd(&p.ws.rb_counter[slot], nch);
-                    last = (old + nch == p.upr);
-                    if (last) atomicExch(&p.ws.rb_counter[slot], 0);
-                }
-                *last_flag = last;
+            if (kq == 0) {
+#pragma unroll
+                for (int o = 1; o < kKSplit; ++o)
+#pragma unroll
+                    for (int t = 0; t < MT; ++t)
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            v[t][i] += sred[((o - 1) * kBM + rg * 16 + g + ((i & 2) ? 8 : 0)) * kMaxTok + 8 * t +
+                                            2 * tq + (i & 1)];
             }
             consumer_bar();
-            finish = *last_flag != 0;
-            if (finish) {
-                __threadfence();
-#pragma unroll
-                for (int t = 0; t < MT; ++t)
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int r = warp * 16 + g + ((i & 2) ? 8 : 0);
-                        const int tok = 8 * t + 2 * tq + (i & 1);
-                        acc[t][i] = atomicExch(&part[r * kMaxTok + tok], 0);
-                    }
-            }
         }
-        if (finish && !*abort_flag) {
-            const int n0 = rb * kBM + warp * 16 + g;
+        if (c0 == 0 && nch == p.upr) {
+            if (!*abort_flag && kq == 0) epilogue(rb, v, sw);
+        } else {
+            if (!*abort_flag && kq == 0) {
+                const int slot = unit_owner(static_cast<long long>(rb) * p.upr, p.units, G);
+                int32_t *part = p.ws.partial + static_cast<size_t>(slot) * (kBM * kMaxTok);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int n = n0 + ((i & 2) ? 8 : 0);
-                if (n >= p.N) continue;
-                const float sw = p.s_w[n];
+                for (int t = 0; t < MT; ++t)
 #pragma unroll
-                for (int t = 0; t < MT; ++t) {
-                    const int tok = 8 * t + 2 * tq + (i & 1);
-                    if (tok >= p.M) continue;
-                    float f = __int2float_rn(acc[t][i]);
-                    f = __fmul_rn(f, p.s_a[tok]);
-                    f = __fmul_rn(f, sw);
-                    const uint16_t b = __bfloat16_as_ushort(__float2bfloat16_rn(f));
-                    if (p.y) p.y[static_cast<size_t>(tok) * p.N + n] = b;
-                    if constexpr (ARGMAX) {
-                        const unsigned long long key = argmax_key(b, n);
-                        if (key > best[t][i & 1]) best[t][i & 1] = key;
+                    for (int i = 0; i < 4; ++i) {
+                        const int r = rg * 16 + g + ((i & 2) ? 8 : 0);
+                        const int tok = 8 * t + 2 * tq + (i & 1);
+                        if (v[t][i] != 0) atomicAdd(&part[r * kMaxTok + tok], v[t][i]);
                     }
-                }
             }
+            pend_rb[npend] = rb;
+            pend_n[npend] = nch;
+            ++npend;
         }
         u += nch;
+    }
+
+    // ------------------------------------------------ settle split row blocks
+    if (npend > 0) {
+        consumer_bar();
+        if (threadIdx.x == 0) {
+            for (int i = 0; i < npend; ++i) {
+                int last = 0;
+                if (!*abort_flag) {
+                    const int slot = unit_owner(static_cast<long long>(pend_rb[i]) * p.upr, p.units, G);
+                    const int old = atom_add_acq_rel_gpu(&p.ws.rb_counter[slot], pend_n[i]);
+                    last = (old + pend_n[i] == p.upr);
+                    if (last) atomicExch(&p.ws.rb_counter[slot], 0);
+                }
+                last_flag[i] = last;
+            }
+        }
+        consumer_bar();
+        for (int i = 0; i < npend; ++i) {
+            if (!last_flag[i] || kq != 0) continue;
+            const int slot = unit_owner(static_cast<long long>(pend_rb[i]) * p.upr, p.units, G);
+            int32_t *part = p.ws.partial + static_cast<size_t>(slot) * (kBM * kMaxTok);
+            int32_t v[MT][4];
+#pragma unroll
+            for (int t = 0; t < MT; ++t)
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int r = rg * 16 + g + ((k & 2) ? 8 : 0);
+                    const int tok = 8 * t + 2 * tq + (k & 1);
+                    v[t][k] = atomicExch(&part[r * kMaxTok + tok], 0);
+                }
+            float swp[2];
+            load_sw(pend_rb[i], swp);
+            epilogue(pend_rb[i], v, swp);
+        }
     }
 
     if constexpr (ARGMAX) {

@@ -146,6 +146,48 @@ __device__ __forceinline__ void mma_s8_16832(int32_t (&d)[4], uint32_t a0, uint3
                  : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// D = A(16x16 f16, row) * B(16x8 f16, col) + D, fp32 accumulate.  Used with
+// integer-valued operands (|v| <= 127): every product is an integer below 2^14
+// and the kernels keep each accumulator below 2^22 before moving it into an
+// int32, a range in which the fp32 tensor-core sum of integers is exact.
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1)
+{
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+                 "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Four int8 values (bytes b0..b3 of v) to two f16x2 words (b0,b1) and (b2,b3),
+// exactly: x + 128 is placed in the low mantissa bits of 1024.0 (f16 0x6400,
+// whose spacing is 1), giving 1024 + 128 + x exactly; subtracting 1152 leaves x.
+__device__ __forceinline__ void i8x4_to_f16x2x2(uint32_t v, uint32_t &lo, uint32_t &hi)
+{
+    const uint32_t u = v ^ 0x80808080u;
+    const uint32_t l = __byte_perm(u, 0x64646464u, 0x4140u);
+    const uint32_t h = __byte_perm(u, 0x64646464u, 0x4342u);
+    const uint32_t bias = 0x64806480u;  // f16x2 (1152, 1152)
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(l), "r"(bias));
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(h), "r"(bias));
+}
+
+// fp32 holding an integer below 2^24 in magnitude -> int32 (exact).
+__device__ __forceinline__ int32_t f2i_exact(float f)
+{
+    return __float2int_rn(f);
+}
+
+// Counter increment with acquire-release semantics at GPU scope.  Used after a
+// CTA barrier: the barrier orders the CTA's earlier global reductions before
+// the release, and the acquire orders the CTA's later reads after it.
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int *p, int v)
+{
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
 // ------------------------------------------------ programmatic dependent launch
 
 // Wait until the grids this one depends on have completed and their memory

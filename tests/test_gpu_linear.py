@@ -133,3 +133,17 @@ def test_workspace_left_zeroed(bi):
     part = ws[256 + 4 * 256 + 8 * 256 * 16:]
     assert int(head.count_nonzero()) == 0 and int(part.count_nonzero()) == 0
     assert bi.bi_workspace_status(ws) == bi.BI_OK
+
+
+def test_packed_weights_equal_separate_calls(bi):
+    """q/k/v (or gate/up) rows stored back to back and run as one call give the
+    same bits as one call per projection: output rows are independent."""
+    K, M = 4096, 5
+    x_np = gen.act_bf16(21, 1, M, K, outliers=gen.outlier_channels(21, K), gain=20.0)
+    q, s = quant_act(bi, x_np)
+    parts = [weights(bi, gen.weight_f32(21, 0, p, n, K), pow2=True) for p, n in ((0, 4096), (1, 1024), (2, 1024))]
+    wq = torch.cat([w for w, _ in parts])
+    sw = torch.cat([v for _, v in parts])
+    packed = linear(bi, q, s, wq, sw, flags=bi.BI_FLAG_PDL)
+    sep = torch.cat([linear(bi, q, s, w, v) for w, v in parts], dim=1)
+    assert torch.equal(packed, sep)
