@@ -169,6 +169,38 @@ BI_API bi_status bi_lmhead_argmax(const int8_t *q, const float *s_a, int M, int 
  */
 BI_API bi_status bi_workspace_status(void *ws, size_t ws_bytes, bi_stream_t stream);
 
+/*
+ * bi_linear_w8a8 for callers that cannot allocate device memory.
+ *
+ * No counterpart in the papers: this is a deployment variant.  Some callers
+ * cannot call cudaMalloc or any allocating routine: code running inside a
+ * custom allocator or memory-pool callback, plugins that their host framework
+ * hands only input and output pointers, and processes that must not grow
+ * their device memory after start-up.  This entry point allocates nothing.
+ * The weight-streaming kernel's scratch (split-K partial sums, their
+ * counters, a status word) is a fixed array of BI_NOALLOC_SCRATCH_BYTES
+ * inside the library, present on every GPU that loads the library until the
+ * process exits.  The caller still passes all inputs and outputs.
+ *
+ *   Arguments, layouts, results and the other errors are those of
+ *   bi_linear_w8a8; there is no workspace argument.
+ *   M must be <= BI_NOALLOC_MAX_M (the most the fixed scratch holds); larger
+ *   M returns BI_ERR_UNSUPPORTED without launching anything.
+ *   The first call on each device looks up the scratch array's device address
+ *   (with that device current); make that first call before any stream
+ *   capture.
+ *   Every call shares the one array: the call clears the parts that must
+ *   start at zero (two cudaMemsetAsync on `stream`) and then launches.  Calls
+ *   that may overlap on the GPU (other streams, other host threads) race on
+ *   the array and must not be issued; calls in order on one stream are fine.
+ *   Results are bitwise identical to bi_linear_w8a8.
+ */
+#define BI_NOALLOC_MAX_M 16
+#define BI_NOALLOC_SCRATCH_BYTES 1082624
+BI_API bi_status bi_linear_w8a8_noalloc(const int8_t *q, const float *s_a, int M, int K,
+                                        const int8_t *w_q, const float *s_w, int N,
+                                        uint16_t *y, unsigned flags, bi_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

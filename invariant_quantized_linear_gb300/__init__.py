@@ -44,6 +44,8 @@ lib.bi_lmhead_argmax.argtypes = [_vp, _vp, _ci, _ci, _vp, _vp, _ci, _vp, _vp, _v
 lib.bi_lmhead_argmax.restype = _ci
 lib.bi_workspace_status.argtypes = [_vp, _sz, _vp]
 lib.bi_workspace_status.restype = _ci
+lib.bi_linear_w8a8_noalloc.argtypes = [_vp, _vp, _ci, _ci, _vp, _vp, _ci, _vp, _cu, _vp]
+lib.bi_linear_w8a8_noalloc.restype = _ci
 
 BI_OK = 0
 BI_ERR_INVALID_ARG = 1
@@ -127,6 +129,17 @@ def bi_lmhead_argmax(q: torch.Tensor, s_a: torch.Tensor, w_q: torch.Tensor, s_w:
     _check(lib.bi_lmhead_argmax(_ptr(q), _ptr(s_a), M, K, _ptr(w_q), _ptr(s_w), N, _ptr(logits),
                                 _ptr(argmax), _ptr(ws), ws.numel() * ws.element_size(), flags,
                                 _stream(stream)), "bi_lmhead_argmax")
+
+
+def bi_linear_w8a8_noalloc(q: torch.Tensor, s_a: torch.Tensor, w_q: torch.Tensor, s_w: torch.Tensor,
+                           y: torch.Tensor, flags: int = 0, stream=None) -> None:
+    """bi_linear_w8a8 without a workspace argument, for callers that cannot
+    allocate device memory: the library keeps the kernel's scratch in a fixed
+    array of its own (M <= 16; calls on one stream only, never overlapping)."""
+    M, K = q.shape
+    N = w_q.shape[0]
+    _check(lib.bi_linear_w8a8_noalloc(_ptr(q), _ptr(s_a), M, K, _ptr(w_q), _ptr(s_w), N, _ptr(y), flags,
+                                      _stream(stream)), "bi_linear_w8a8_noalloc")
 
 
 def bi_workspace_status(ws: torch.Tensor, stream=None) -> int:
