@@ -54,6 +54,8 @@ def parse():
     p.add_argument("--layers", type=int, default=36)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-sweep", action="store_true", help="skip the per-M sweep")
+    p.add_argument("--mode", default="program", choices=["program", "calls"],
+                   help="program: the step as one verify-pass program launch; calls: one launch per op")
     return p.parse_args()
 
 
@@ -192,7 +194,30 @@ class Stack:
             torch.cuda.synchronize()
         return wq, sw
 
-    def launches_per_step(self):
+    def build_program(self, M):
+        """The step as one verify-pass program (bi_program_*): the same ops,
+        in the same order, each starting after all earlier ones."""
+        bi = self.bi
+        ops = []
+        s = self.s[:M]
+        for l in range(self.layers):
+            for nm, K in self.in_dims:
+                qbuf = self.q.view(-1)[:M * K].view(M, K)
+                ops.append(bi.op_quantize_act(self.x[(l, nm)][:M, :K], qbuf, s, K=K))
+                wq, sw = self.W[l][nm]
+                ops.append(bi.op_linear(qbuf, s, wq, sw, self.y[nm][:M]))
+        K = 4096
+        qbuf = self.q.view(-1)[:M * K].view(M, K)
+        ops.append(bi.op_quantize_act(self.x[("head",)][:M], qbuf, s, K=K))
+        wq, sw = self.head
+        ops.append(bi.op_lmhead(qbuf, s, wq, sw, None, self.argmax[:M]))
+        prog = bi.new_program(len(ops), device=self.dev)
+        bi.bi_program_build(ops, prog)
+        return prog
+
+    def launches_per_step(self, mode="calls"):
+        if mode == "program":
+            return 1
         return self.layers * 2 * len(self.groups) + 2
 
     def linear_bytes(self, M):
@@ -202,6 +227,19 @@ class Stack:
             for nm, K in self.in_dims:
                 N = self.W[l][nm][0].shape[0]
                 tot += N * K + 4 * N + M * K + 4 * M + 2 * M * N
+        return tot
+
+    def step_bytes(self, M):
+        """Algorithmic bytes of one step: every linear's W + s_w + q + s_a + y,
+        every quantisation's x read and q + s_a written, the head's W + s_w +
+        q + s_a and argmax."""
+        tot = self.linear_bytes(M)
+        for l in range(self.layers):
+            for nm, K in self.in_dims:
+                tot += 2 * M * K + M * K + 4 * M
+        N, K = self.head[0].shape
+        tot += 2 * M * K + M * K + 4 * M
+        tot += N * K + 4 * N + M * K + 4 * M + 4 * M
         return tot
 
     def step(self, M, flags, linears_only=False):
@@ -253,13 +291,24 @@ def run_ours(args):
             torch.distributed.barrier()
         torch.cuda.synchronize()
 
+    progs = {}
+    prog_ws = torch.zeros(bi.bi_program_workspace_size(), dtype=torch.uint8, device=dev)
+
+    def enqueue_step(m):
+        if args.mode == "program":
+            if m not in progs:
+                progs[m] = st.build_program(m)
+            bi.bi_program_run(progs[m], m, prog_ws)
+        else:
+            st.step(m, flags)
+
     def graph_for(m):
         with torch.cuda.stream(stream):
-            st.step(m, flags)          # warm-up outside capture (tensor maps, attributes)
+            enqueue_step(m)            # warm-up outside capture (tensor maps, attributes)
         stream.synchronize()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
-            st.step(m, flags)
+            enqueue_step(m)
         return g
 
     def time_graph(g, steps, warmup):
@@ -297,18 +346,31 @@ def run_ours(args):
                              "weight_gbs": round(st.weight_bytes / (msm * 1e-3) / 1e9, 1),
                              "tokens_per_s_eq": round(m / (msm * 1e-3), 1)}
 
-    # dominant kernel: the step's weight-streaming linear launches alone,
-    # back to back in a CUDA graph (same launch configuration as the step),
-    # timed with events on the launching stream
-    with torch.cuda.stream(stream):
-        st.step(M, flags, linears_only=True)
-    stream.synchronize()
-    gl = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(gl, stream=stream):
-        st.step(M, flags, linears_only=True)
-    lin_launches = st.layers * len(st.groups)
-    lin_ms = time_graph(gl, max(5, args.steps // 2), 3)
-    achieved = st.linear_bytes(M) / (lin_ms * 1e-3) / 1e9
+    if args.mode == "program":
+        # dominant kernel: the program kernel itself, one launch per step;
+        # its average duration is the step time measured above
+        kernel_name = "program_kernel (bi_program_run, M<=16)"
+        lin_launches = 1
+        lin_ms = ms
+        achieved = st.step_bytes(M) / (ms * 1e-3) / 1e9
+        note = ("achieved = algorithmic bytes of the step (all weights and scales, activations read and "
+                "written, outputs) / the program launch's event-timed duration")
+    else:
+        # dominant kernel: the step's weight-streaming linear launches alone,
+        # back to back in a CUDA graph (same launch configuration as the step),
+        # timed with events on the launching stream
+        with torch.cuda.stream(stream):
+            st.step(M, flags, linears_only=True)
+        stream.synchronize()
+        gl = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gl, stream=stream):
+            st.step(M, flags, linears_only=True)
+        kernel_name = "skinny_kernel (bi_linear_w8a8, M<=16)"
+        lin_launches = st.layers * len(st.groups)
+        lin_ms = time_graph(gl, max(5, args.steps // 2), 3)
+        achieved = st.linear_bytes(M) / (lin_ms * 1e-3) / 1e9
+        note = ("achieved = algorithmic bytes (W + s_w + q + s_a + y) of the step's %d linear launches / "
+                "their event-timed duration back to back in a CUDA graph" % lin_launches)
 
     # end to end: activations H2D from pinned memory, graph, argmax D2H
     host_x = {k: torch.from_numpy(v.view(np.int16)).pin_memory() for k, v in st.x_np.items()}
@@ -332,9 +394,10 @@ def run_ours(args):
 
     peaks, kind = read_peaks()
     peak = float(peaks["hbm_gbs"])
-    skinny_src = os.path.join(ROOT, "invariant_quantized_linear_gb300", "csrc", "k_skinny.cu")
+    src = os.path.join(ROOT, "invariant_quantized_linear_gb300", "csrc",
+                       "k_program.cu" if args.mode == "program" else "k_skinny.cu")
     traffic = None
-    if NCU_TRAFFIC["source_sha256"] == source_sha(skinny_src):
+    if NCU_TRAFFIC["source_sha256"] == source_sha(src):
         traffic = NCU_TRAFFIC["bytes_per_launch"]
 
     cpu = cpu_baseline(bounded_s=12.0) if rank == 0 else None
@@ -350,21 +413,21 @@ def run_ours(args):
                        "l2": "inputs larger than L2 (all weights read once per step)",
                        "activations": "independent synthetic input per linear group (layers not chained)",
                        "packing": "q/k/v and gate/up weight rows packed: one call per group",
-                       "launch": "CUDA graph of the step, programmatic dependent launch",
+                       "launch": ("one verify-pass program launch per step (persistent cooperative kernel, "
+                                  "grid barrier between ops), in a CUDA graph" if args.mode == "program" else
+                                  "CUDA graph of the step, one launch per op, programmatic dependent launch"),
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "pct_of_hbm_copy": round(100 * gbs / world / peak, 1),
             "tokens_per_s_eq": round(M * world / (ms * 1e-3), 1),
             "per_m": per_m,
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": traffic,
-                         "kernel": "skinny_kernel (bi_linear_w8a8, M<=16)",
+                         "kernel": kernel_name,
                          "launch_us": round(lin_ms * 1e3 / lin_launches, 3),
-                         "peak_kind": kind, "note": "achieved = algorithmic bytes (W + s_w + q + s_a + y) "
-                                                   "of the step's %d linear launches / their event-timed "
-                                                   "duration back to back in a CUDA graph" % lin_launches},
+                         "peak_kind": kind, "note": note},
             "e2e": {"value": round(e2e_gbs, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": 4 * M, "ms_per_step": round(e2e_ms, 4)},
-            "gpu_launches": st.launches_per_step() * args.steps,
+            "gpu_launches": st.launches_per_step(args.mode) * args.steps,
             "clocks": clk,
             "cpu_baseline": cpu,
             "setup_s": round(setup_s, 1),

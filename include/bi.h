@@ -170,6 +170,57 @@ BI_API bi_status bi_lmhead_argmax(const int8_t *q, const float *s_a, int M, int 
 BI_API bi_status bi_workspace_status(void *ws, size_t ws_bytes, bi_stream_t stream);
 
 /*
+ * Verify-pass executor: a program of ops run by one persistent kernel.
+ *
+ * A decode or verify pass is a chain of small dependent steps (quantise an
+ * activation, stream a weight matrix, ...).  Launched one call at a time each
+ * step pays a launch, a ramp to full memory bandwidth and a tail, which for
+ * the smaller projections cost more than the weight read itself.  A program
+ * runs all of them in one cooperative launch (one CTA per SM): op i starts
+ * only after every op before it has completed on the whole GPU (a grid-wide
+ * barrier), so an op may read anything earlier ops wrote, while the weight
+ * tiles of the ops ahead keep streaming into shared memory across the
+ * barriers (weights never depend on earlier ops).  Every op gives exactly
+ * the bits of the corresponding single call.
+ *
+ * Build once, run many times: bi_program_build validates the ops, encodes
+ * the TMA descriptors and copies the program (bi_program_bytes(n_ops) bytes,
+ * caller-allocated device memory, 128-byte aligned) synchronously; the
+ * program refers to the ops' buffers by address, so their contents may
+ * change between runs but not their addresses.  bi_program_run is one
+ * asynchronous launch on `stream` (capturable in a CUDA graph once the
+ * program is built); `max_tokens` is the largest M of the program's linear
+ * and LM-head ops (1..16) and must be the value the program was built for.
+ * The workspace follows the zero-fill rule of bi_linear_workspace_size.
+ * A mismatched program or max_tokens is reported by bi_workspace_status as
+ * BI_ERR_INVALID_ARG; a bounded wait that gives up as BI_ERR_TIMEOUT.
+ */
+typedef enum {
+    BI_OP_QUANTIZE_ACT = 1, /* x, ldx, M, K -> q, s_a        (bi_quantize_act)  */
+    BI_OP_LINEAR = 2,       /* q, s_a, M, K, w_q, s_w, N -> y (bi_linear_w8a8, M <= 16) */
+    BI_OP_LMHEAD = 3        /* ... -> y (logits, may be NULL), argmax (bi_lmhead_argmax) */
+} bi_op_kind;
+
+typedef struct {
+    int kind;               /* bi_op_kind */
+    int M, N, K;            /* N unused by BI_OP_QUANTIZE_ACT */
+    const uint16_t *x;      /* BI_OP_QUANTIZE_ACT input rows */
+    int64_t ldx;
+    int8_t *q;              /* quantise: output; linear / head: input */
+    float *s_a;             /* quantise: output; linear / head: input */
+    const int8_t *w_q;      /* linear / head weights [N, K] */
+    const float *s_w;       /* [N] */
+    uint16_t *y;            /* linear: output [M, N]; head: logits or NULL */
+    int32_t *argmax;        /* head: output [M] */
+} bi_op;
+
+BI_API size_t bi_program_bytes(int n_ops);
+BI_API size_t bi_program_workspace_size(void);
+BI_API bi_status bi_program_build(const bi_op *ops, int n_ops, void *program, size_t program_bytes);
+BI_API bi_status bi_program_run(const void *program, int max_tokens, void *ws, size_t ws_bytes,
+                                bi_stream_t stream);
+
+/*
  * bi_linear_w8a8 for callers that cannot allocate device memory.
  *
  * No counterpart in the papers: this is a deployment variant.  Some callers

@@ -47,6 +47,28 @@ lib.bi_workspace_status.restype = _ci
 lib.bi_linear_w8a8_noalloc.argtypes = [_vp, _vp, _ci, _ci, _vp, _vp, _ci, _vp, _cu, _vp]
 lib.bi_linear_w8a8_noalloc.restype = _ci
 
+lib.bi_program_bytes.argtypes = [_ci]
+lib.bi_program_bytes.restype = _sz
+lib.bi_program_workspace_size.argtypes = []
+lib.bi_program_workspace_size.restype = _sz
+
+
+class bi_op(ctypes.Structure):
+    """One op of a verify-pass program (struct bi_op of include/bi.h)."""
+    _fields_ = [("kind", _ci), ("M", _ci), ("N", _ci), ("K", _ci),
+                ("x", _vp), ("ldx", _i64), ("q", _vp), ("s_a", _vp),
+                ("w_q", _vp), ("s_w", _vp), ("y", _vp), ("argmax", _vp)]
+
+
+lib.bi_program_build.argtypes = [ctypes.POINTER(bi_op), _ci, _vp, _sz]
+lib.bi_program_build.restype = _ci
+lib.bi_program_run.argtypes = [_vp, _ci, _vp, _sz, _vp]
+lib.bi_program_run.restype = _ci
+
+BI_OP_QUANTIZE_ACT = 1
+BI_OP_LINEAR = 2
+BI_OP_LMHEAD = 3
+
 BI_OK = 0
 BI_ERR_INVALID_ARG = 1
 BI_ERR_ALIGNMENT = 2
@@ -140,6 +162,53 @@ def bi_linear_w8a8_noalloc(q: torch.Tensor, s_a: torch.Tensor, w_q: torch.Tensor
     N = w_q.shape[0]
     _check(lib.bi_linear_w8a8_noalloc(_ptr(q), _ptr(s_a), M, K, _ptr(w_q), _ptr(s_w), N, _ptr(y), flags,
                                       _stream(stream)), "bi_linear_w8a8_noalloc")
+
+
+def bi_program_bytes(n_ops: int) -> int:
+    return int(lib.bi_program_bytes(n_ops))
+
+
+def bi_program_workspace_size() -> int:
+    return int(lib.bi_program_workspace_size())
+
+
+def bi_program_build(ops, program: torch.Tensor) -> None:
+    """ops: a sequence of bi_op; program: device uint8 tensor of at least
+    bi_program_bytes(len(ops)) bytes, 128-byte aligned."""
+    arr = (bi_op * len(ops))(*ops)
+    _check(lib.bi_program_build(arr, len(ops), _ptr(program), program.numel() * program.element_size()),
+           "bi_program_build")
+
+
+def bi_program_run(program: torch.Tensor, max_tokens: int, ws: torch.Tensor, stream=None) -> None:
+    _check(lib.bi_program_run(_ptr(program), max_tokens, _ptr(ws), ws.numel() * ws.element_size(),
+                              _stream(stream)), "bi_program_run")
+
+
+def op_quantize_act(x: torch.Tensor, q: torch.Tensor, s_a: torch.Tensor, K: int | None = None) -> bi_op:
+    M = x.shape[0]
+    K = x.shape[1] if K is None else K
+    return bi_op(BI_OP_QUANTIZE_ACT, M, 0, K, _ptr(x), x.stride(0), _ptr(q), _ptr(s_a), None, None, None, None)
+
+
+def op_linear(q: torch.Tensor, s_a: torch.Tensor, w_q: torch.Tensor, s_w: torch.Tensor, y: torch.Tensor) -> bi_op:
+    M, K = q.shape
+    return bi_op(BI_OP_LINEAR, M, w_q.shape[0], K, None, 0, _ptr(q), _ptr(s_a), _ptr(w_q), _ptr(s_w), _ptr(y), None)
+
+
+def op_lmhead(q: torch.Tensor, s_a: torch.Tensor, w_q: torch.Tensor, s_w: torch.Tensor,
+              logits: torch.Tensor | None, argmax: torch.Tensor) -> bi_op:
+    M, K = q.shape
+    return bi_op(BI_OP_LMHEAD, M, w_q.shape[0], K, None, 0, _ptr(q), _ptr(s_a), _ptr(w_q), _ptr(s_w),
+                 _ptr(logits), _ptr(argmax))
+
+
+def new_program(n_ops: int, device="cuda") -> torch.Tensor:
+    """Device memory for a program of n_ops ops (128-byte aligned)."""
+    n = bi_program_bytes(n_ops)
+    buf = torch.empty(n + 128, dtype=torch.uint8, device=device)
+    off = (-buf.data_ptr()) % 128
+    return buf[off:off + n]
 
 
 def bi_workspace_status(ws: torch.Tensor, stream=None) -> int:

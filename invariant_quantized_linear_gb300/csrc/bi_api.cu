@@ -257,7 +257,7 @@ bi_status bi_workspace_status(void *ws, size_t ws_bytes, bi_stream_t stream)
     if (word == bi::DEV_OK) return BI_OK;
     const int zero = 0;
     if (cudaMemcpy(ws, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return BI_ERR_CUDA;
-    return BI_ERR_TIMEOUT;
+    return word == bi::DEV_BAD_PROGRAM ? BI_ERR_INVALID_ARG : BI_ERR_TIMEOUT;
 }
 
 }  // extern "C"

@@ -29,6 +29,7 @@
 // complement of faults F1-F5).
 #include "kernels.cuh"
 #include "ptx.cuh"
+#include "stream_mma.cuh"
 
 #include <cuda_bf16.h>
 
@@ -36,13 +37,11 @@ namespace bi {
 
 namespace {
 
-constexpr int kRowGroups = 4;                       // 16-row groups per 64-row block
-constexpr int kKSplit = 2;                          // warps sharing one row group's K
-constexpr int kConsumerWarps = kRowGroups * kKSplit;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kNch = 2;                    // 128-byte chunks of K per unit
-constexpr int kUnitK = kNch * 128;         // bytes of K per unit
-constexpr int kWChunkBytes = kBM * 128;    // 8 KB: 64 rows x 128 B
+using namespace stream;
+using Gs = Geo<2>;   // eight consumer warps: two CTAs fit on one SM
+constexpr int kKSplit = Gs::kKSplit;
+constexpr int kConsumerWarps = Gs::kConsumerWarps;
+constexpr int kThreads = Gs::kThreads;
 
 template <int MT>
 struct Cfg {
@@ -67,28 +66,6 @@ struct Params {
     Workspace ws;
     int pdl;
 };
-
-__device__ __forceinline__ long long range_start(long long i, long long units, int G)
-{
-    return (i * units) / G;
-}
-
-// CTA whose range holds unit u: the largest i with range_start(i) <= u.
-__device__ __forceinline__ int unit_owner(long long u, long long units, int G)
-{
-    return static_cast<int>(((u + 1) * G - 1) / units);
-}
-
-// Which 32-byte groups of K run on the int8 MMA (no conversion; a separate,
-// slower pipe) and which on the f16 MMA (fast, but each int8 operand is first
-// converted): splitting the groups keeps both pipes and the ALU below their
-// limits at HBM speed.  With two token tiles the int8 MMA does twice the work
-// per group, so it takes a smaller share.
-template <int MT>
-__device__ __forceinline__ constexpr bool imma_group(int t)
-{
-    return MT == 1 ? (t & 1) == 0 : (t & 3) == 0;
-}
 
 __device__ __forceinline__ void consumer_bar()
 {
@@ -219,15 +196,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     // ---------------------------------------------------------------- consumers
     if (p.pdl) pdl_wait();
-    const int g = lane >> 2, tq = lane & 3;
-    const int mat = lane >> 3, r8 = lane & 7;
-    // ldmatrix row addresses: weight rows for the A operand, token rows for B
-    const int rg = warp % kRowGroups;   // 16-row group inside the row block
-    const int kq = warp / kRowGroups;   // which share of each stage's K this warp takes
-    const uint32_t a_row = rg * 16 + ((mat & 1) ? 8 : 0) + r8;
-    const int a_hi = (mat & 2) ? 1 : 0;                    // chunk X or Y
-    const uint32_t b_tok = (MT == 2 && (lane >> 4)) ? 8 + r8 : r8;
-    const int b_hi = (lane >> 3) & 1;
+    const Lane L = lane_setup<MT, kKSplit>(warp, lane);
+    const int g = L.g, tq = L.tq, rg = L.rg, kq = L.kq;
 
     unsigned long long best[MT][2];
 #pragma unroll
@@ -301,67 +271,11 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
                 continue;
             }
-            const uint32_t wbase = smem_u32(sW + s * C::kWStage);
-            const uint32_t abase = smem_u32(sA + s * C::kAStage);
-            // All int8 fragments of the stage first (the loads overlap), then
-            // exact int8 -> f16 conversion and f16 tensor-core MMAs into two
-            // fp32 accumulators.  One ldmatrix group covers 32 bytes of K:
-            // A regs r0/r1 = rows g / g+8 of 16-byte chunk X, r2/r3 = chunk Y;
-            // B regs = token rows of chunks X and Y.  Logical k of the MMA is
-            // a fixed permutation of the bytes, identical for A and B, so the
-            // integer dot product is unchanged.
-            constexpr int kGroups = kNch * 4 / kKSplit;   // 32-byte groups of K per warp per stage
-            uint32_t fa[kGroups][4];
-            uint32_t fb[kGroups][2 * MT];
-#pragma unroll
-            for (int tt = 0; tt < kGroups; ++tt) {
-                const int t = kq * kGroups + tt;
-                const int ch = t >> 2, ks = t & 3;
-                ldmatrix_x4(wbase + ch * kWChunkBytes + swz128(a_row, 2 * ks + a_hi), fa[tt][0], fa[tt][1],
-                            fa[tt][2], fa[tt][3]);
-                if constexpr (MT == 1)
-                    ldmatrix_x2(abase + ch * C::kAChunkBytes + swz128(b_tok, 2 * ks + b_hi), fb[tt][0], fb[tt][1]);
-                else
-                    ldmatrix_x4(abase + ch * C::kAChunkBytes + swz128(b_tok, 2 * ks + b_hi), fb[tt][0], fb[tt][1],
-                                fb[tt][2], fb[tt][3]);
-            }
-            float facc[2][MT][4];
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-#pragma unroll
-                for (int m = 0; m < MT; ++m) facc[h][m][0] = facc[h][m][1] = facc[h][m][2] = facc[h][m][3] = 0.0f;
-#pragma unroll
-            for (int t = 0; t < kGroups; ++t) {
-                if (imma_group<MT>(t)) {
-                    // int8 tensor-core MMA on the raw codes, straight into int32
-#pragma unroll
-                    for (int m = 0; m < MT; ++m)
-                        mma_s8_16832(v[m], fa[t][0], fa[t][1], fa[t][2], fa[t][3], fb[t][2 * m], fb[t][2 * m + 1]);
-                    continue;
-                }
-#pragma unroll
-                for (int xy = 0; xy < 2; ++xy) {   // chunk X, then chunk Y
-                    uint32_t a0, a1, a2, a3;
-                    i8x4_to_f16x2x2(fa[t][2 * xy], a0, a2);      // row g
-                    i8x4_to_f16x2x2(fa[t][2 * xy + 1], a1, a3);  // row g + 8
-#pragma unroll
-                    for (int m = 0; m < MT; ++m) {
-                        uint32_t b0, b1;
-                        i8x4_to_f16x2x2(fb[t][2 * m + xy], b0, b1);
-                        mma_f16_16816(facc[xy][m], a0, a1, a2, a3, b0, b1);
-                    }
-                }
-            }
+            consume_stage<MT, kKSplit>(smem_u32(sW + s * C::kWStage), smem_u32(sA + s * C::kAStage), C::kAChunkBytes, L, v);
             // every fragment has been consumed by an issued MMA, so the
             // stage's shared memory has been read: hand it back
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
-            // per stage each fp32 partial covers at most 64 bytes of K: an
-            // integer of magnitude <= 64 * 127^2 < 2^20, moved exactly into int32
-#pragma unroll
-            for (int m = 0; m < MT; ++m)
-#pragma unroll
-                for (int i = 0; i < 4; ++i) v[m][i] += f2i_exact(facc[0][m][i]) + f2i_exact(facc[1][m][i]);
         }
 
         // the kKSplit warps of a row group hold partial sums of the same

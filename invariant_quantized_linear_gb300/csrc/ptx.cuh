@@ -10,7 +10,7 @@
 namespace bi {
 
 // Status word values written by kernels into a workspace.
-enum : int { DEV_OK = 0, DEV_TIMEOUT = 1 };
+enum : int { DEV_OK = 0, DEV_TIMEOUT = 1, DEV_BAD_PROGRAM = 2 };
 
 // A bounded wait gives up after this many nanoseconds of the global timer.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
@@ -72,6 +72,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
+// Non-blocking test of the phase with the given parity (never suspends).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok)
+                 : "r"(smem_u32(bar)), "r"(parity)
+                 : "memory");
+    return ok != 0;
+}
+
 // Wait for the phase with the given parity to complete.  Gives up (returns
 // false) after kWaitLimitNs, or as soon as *abort becomes non-zero.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, volatile int *abort)
@@ -115,6 +128,16 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, u
         " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "l"(policy)
         : "memory");
+}
+
+// Prefetch one 2-D box of a tensor into L2 (no shared memory, no completion
+// signal); a later tma_load_2d of the same box then reads it from L2.
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int x, int y)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y)
+                 : "memory");
 }
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map)
@@ -170,6 +193,23 @@ __device__ __forceinline__ void i8x4_to_f16x2x2(uint32_t v, uint32_t &lo, uint32
     const uint32_t bias = 0x64806480u;  // f16x2 (1152, 1152)
     asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(l), "r"(bias));
     asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(h), "r"(bias));
+}
+
+// Per-element activation code clamp(rne(v / s), -127, 127) with v / s an IEEE
+// division, computed as v * r with r = 1/s correctly rounded, and checked.
+// With |v / s| <= 127.0001, the product v * r differs from the rounded
+// quotient fl(v / s) by less than 3 * 2^-24 * 127.0001 < 2.3e-5 (three
+// roundings of relative size <= 2^-24 each), so both round to the same
+// integer unless the product lies within that distance of a half-integer.
+// Products within 2^-10 of a half-integer take the exact division instead.
+__device__ __forceinline__ int quant_code(float v, float s, float r)
+{
+    const float t = __fmul_rn(v, r);
+    int k = __float2int_rn(t);
+    const float d = fabsf(t - static_cast<float>(k));   // exact: |t| < 2^8
+    // (also taken when r overflowed for a tiny subnormal s: t is then inf or NaN)
+    if (!(d < 0.5f - 0.0009765625f)) k = __float2int_rn(__fdiv_rn(v, s));
+    return max(-127, min(127, k));
 }
 
 // fp32 holding an integer below 2^24 in magnitude -> int32 (exact).
