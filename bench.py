@@ -27,6 +27,7 @@ import json
 import os
 import statistics
 import subprocess
+import threading
 import sys
 import time
 
@@ -48,7 +49,7 @@ NCU_TRAFFIC = {"source_sha256": None, "bytes_per_launch": None, "launch": None}
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--steps", type=int, default=100)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--m", type=int, default=8, help="tokens per verify pass (1..16)")
     p.add_argument("--layers", type=int, default=36)
@@ -75,49 +76,69 @@ def read_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi samples during the timed region (clocks and throttle reasons)."""
+    """nvidia-smi samples (clocks and throttle reasons), each stamped with the
+    host time it arrived, so that the ones taken during the timed region can be
+    picked out afterwards."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    PERIOD_MS = 50
 
     def __init__(self, gpu_index: int):
+        self.samples = []
         self.proc = None
-        self.gpu = gpu_index
+        self.first = threading.Event()
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(gpu_index), "--query-gpu=" + self.FIELDS,
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", str(self.PERIOD_MS)],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
-            self.proc = None
+            return
+        self.reader = threading.Thread(target=self._read, daemon=True)
+        self.reader.start()
+        self.first.wait(timeout=10.0)        # sampling is running before the timed region
 
-    def stop(self):
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.monotonic(), line))
+            self.first.set()
+
+    def stop(self, t0, t1):
+        """Summary of the samples taken in [t0, t1] (host monotonic seconds); if
+        the region was shorter than the sampling period, the first sample after
+        t0."""
         if self.proc is None:
             return None
         self.proc.terminate()
         try:
-            out, _ = self.proc.communicate(timeout=5)
+            self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-            out, _ = self.proc.communicate()
-        sm, smax, reasons = [], [], set()
+            self.proc.wait()
+        self.reader.join(timeout=5)
+        rows = []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in out.splitlines():
+        for t, line in self.samples:
             f = [c.strip() for c in line.split(",")]
             if len(f) < 9:
                 continue
             try:
-                sm.append(float(f[1]))
-                smax.append(float(f[2]))
+                rows.append((t, float(f[1]), float(f[2]),
+                             {n for n, v in zip(names, f[5:9]) if v.lower() == "active"}))
             except ValueError:
                 continue
-            for name, v in zip(names, f[5:9]):
-                if v.lower() == "active":
-                    reasons.add(name)
-        if not sm:
+        inside = [r for r in rows if t0 <= r[0] <= t1]
+        window = "timed region"
+        if not inside:
+            after = [r for r in rows if r[0] >= t0]
+            inside = after[:1]
+            window = "first sample after the timed region began"
+        if not inside:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        reasons = set().union(*(r[3] for r in inside))
+        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": sorted(reasons), "samples": len(inside), "window": window}
 
 
 # ------------------------------------------------------------------- model
@@ -311,10 +332,13 @@ def run_ours(args):
             enqueue_step(m)
         return g
 
+    region = {}
+
     def time_graph(g, steps, warmup):
         for _ in range(warmup):
             g.replay()
         barrier()
+        region["t0"] = time.monotonic()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):
@@ -323,6 +347,7 @@ def run_ours(args):
                 g.replay()
             e1.record(stream)
         barrier()
+        region["t1"] = time.monotonic()
         ms = e0.elapsed_time(e1) / steps
         if world > 1:
             t = torch.tensor([ms], device=dev)
@@ -333,7 +358,7 @@ def run_ours(args):
     g = graph_for(M)
     clocks = ClockSampler(local)
     ms = time_graph(g, args.steps, args.warmup)
-    clk = clocks.stop()
+    clk = clocks.stop(region["t0"], region["t1"])
     gbs = st.weight_bytes * world / (ms * 1e-3) / 1e9
 
     # per-M sweep (same step, fewer repetitions)

@@ -225,7 +225,10 @@ __global__ void __launch_bounds__(kThreads, 2) program_kernel(const ProgHeader *
                     if (qw > 0) seen_q = ld_acquire_gpu(ws.qdone);
                     fence_proxy_async_global();
                     refreshed = true;
-                    if ((b > 0 && seen < b * G) || (qw > 0 && seen_q < qw)) return;
+                    if ((b > 0 && seen < b * G) || (qw > 0 && seen_q < qw)) {
+                        __nanosleep(128);   // back off: every CTA polls the same counters
+                        return;
+                    }
                 }
 #pragma unroll
                 for (int ch = 0; ch < kNch; ++ch)
@@ -309,6 +312,7 @@ __global__ void __launch_bounds__(kThreads, 2) program_kernel(const ProgHeader *
             const unsigned long long t0 = global_timer_ns();
             int spins = 0;
             while (ld_acquire_gpu(ws.bar) < b * G) {
+                __nanosleep(64);
                 if ((++spins & 63) == 0 && (*abort_flag || global_timer_ns() - t0 > kWaitLimitNs)) {
                     fail();
                     break;
@@ -326,6 +330,7 @@ __global__ void __launch_bounds__(kThreads, 2) program_kernel(const ProgHeader *
                 const unsigned long long t0 = global_timer_ns();
                 int spins = 0;
                 while (ld_acquire_gpu(ws.qdone) < op.qwait) {
+                    __nanosleep(64);
                     if ((++spins & 63) == 0 && (*abort_flag || global_timer_ns() - t0 > kWaitLimitNs)) {
                         fail();
                         break;
