@@ -38,6 +38,10 @@ def lib():
         L.oracle_linear_w8a8.restype = ci
         L.oracle_lmhead_argmax.argtypes = [vp, vp, ci, ci, vp, vp, ci, vp, vp]
         L.oracle_lmhead_argmax.restype = ci
+        L.oracle_residual_rescale.argtypes = [vp, vp, i64, ci, ci]
+        L.oracle_residual_rescale.restype = None
+        L.oracle_relu_mul.argtypes = [vp, i64, ci, ci, vp]
+        L.oracle_relu_mul.restype = None
         L.oracle_num_threads.argtypes = []
         L.oracle_num_threads.restype = ci
         _LIB = L
@@ -130,6 +134,64 @@ def lmhead_argmax(q, s_a, wq, s_w, want_logits: bool = True):
     if rc != 0:
         raise OverflowError("an int8 dot product reached 2^31")
     return am, logits
+
+
+def residual_rescale(h: np.ndarray, y: np.ndarray) -> np.ndarray:
+    """New residual stream: bf16_rne(h + y) rescaled by 2^-ilogb(row absmax).
+    h: uint16 [M, K]; y: uint16 [M, >= K] (the first K columns are added)."""
+    out = np.array(_c(h, np.uint16), copy=True)
+    y = _c(y, np.uint16)
+    M, K = out.shape
+    assert y.shape[0] == M and y.shape[1] >= K
+    lib().oracle_residual_rescale(out.ctypes.data, y.ctypes.data, y.shape[1], M, K)
+    return out
+
+
+def relu_mul(gu: np.ndarray, K: int) -> np.ndarray:
+    """bf16_rne(relu(g) * u) for g = gu[:, :K], u = gu[:, K:2K]; uint16 [M, K]."""
+    gu = _c(gu, np.uint16)
+    M, ld = gu.shape
+    assert ld >= 2 * K
+    out = np.empty((M, K), np.uint16)
+    lib().oracle_relu_mul(gu.ctypes.data, ld, M, K, out.ctypes.data)
+    return out
+
+
+def verify_pass(h0: np.ndarray, layers, head, q_rows: int, record: bool = False):
+    """Chained verify pass over a stack of W8A8 layers, then the greedy head.
+
+    h0: uint16 [M, H] bf16 residual stream entering layer 0.
+    layers: sequence of dicts with int8 codes and fp32 scales
+        "qkv": (wq [q_rows + 2*kv, H], s_w)  q, k, v rows packed in that order
+        "o": (wq [H, q_rows], s_w), "gu": (wq [2*I, H], s_w)  gate rows then up rows,
+        "down": (wq [H, I], s_w).
+    head: (wq [V, H], s_w).
+    Per layer:  q_h = quant(h);  y_qkv = lin(q_h, qkv);  a = y_qkv[:, :q_rows]
+    (attention stand-in; k and v are computed and returned, not used);
+    h = residual_rescale(h, lin(quant(a), o));  y_gu = lin(quant(h), gu);
+    h = residual_rescale(h, lin(quant(relu_mul(y_gu)), down)).
+    Then argmax = head(quant(h)).  Returns (argmax int32 [M], h, records) with
+    records, if asked, the per-layer dict of every linear output and h."""
+    h = np.array(_c(h0, np.uint16), copy=True)
+    recs = []
+    for L in layers:
+        q, s = quantize_act(h)
+        y_qkv = linear_w8a8(q, s, *L["qkv"])
+        qa, sa = quantize_act(np.ascontiguousarray(y_qkv[:, :q_rows]))
+        y_o = linear_w8a8(qa, sa, *L["o"])
+        h = residual_rescale(h, y_o)
+        h_mid = h
+        q, s = quantize_act(h)
+        y_gu = linear_w8a8(q, s, *L["gu"])
+        inter = L["gu"][0].shape[0] // 2
+        mq, ms = quantize_act(relu_mul(y_gu, inter))
+        y_d = linear_w8a8(mq, ms, *L["down"])
+        h = residual_rescale(h, y_d)
+        if record:
+            recs.append({"qkv": y_qkv, "o": y_o, "h_mid": h_mid, "gu": y_gu, "down": y_d, "h": h})
+    q, s = quantize_act(h)
+    am, _ = lmhead_argmax(q, s, *head, want_logits=False)
+    return am, h, recs
 
 
 def num_threads() -> int:

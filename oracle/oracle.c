@@ -252,6 +252,70 @@ int oracle_lmhead_argmax(const int8_t *q, const float *s_a, int M, int K,
     return rc;
 }
 
+/* ------------------------------------------- chained verify pass (elementwise)
+ *
+ * The pages measure a decode/verify pass as a chain of layers whose linears
+ * read the previous ones' outputs ([cintu] "the mat-vec kernel", [goyal]
+ * "The physics"), but print no layer body.  Reading (no attention): the q
+ * slice of the packed q/k/v output stands in for the attention output; the
+ * residual stream h is updated twice per layer; the MLP gate is a ReLU (no
+ * transcendental, so both sides round identically).  Each step below is one
+ * IEEE fp32 operation on bf16 inputs followed by one bf16 rounding.  Because
+ * fp32 has 24 >= 2*8+2 significand bits, an fp32 add or multiply of bf16
+ * values followed by bf16 rounding equals a single rounding of the exact
+ * result, so these have a plain definition (checked against exact rationals).
+ */
+
+/*
+ * Residual add with a power-of-two row rescale, in place on h [M, K] (row
+ * stride K):  h' = bf16_rne(h + y)  (fp32 add);  e = ilogb(max_k |h'|)
+ * (e = 0 for an all-zero row);  h = bf16_rne(h' * 2^-e).  The rescale keeps a
+ * 36-layer stack finite and changes no quantisation code: per-row absmax
+ * quantisation is exactly invariant to multiplying a row by a power of two.
+ * The product is formed in double (exact) and rounded to fp32 then bf16; it is
+ * exact except below 2^-142, where both roundings give a signed zero.
+ */
+void oracle_residual_rescale(uint16_t *h, const uint16_t *y, int64_t ldy, int M, int K)
+{
+    uint16_t *t = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)K);
+    for (int m = 0; m < M; ++m) {
+        uint16_t *hr = h + (int64_t)m * K;
+        const uint16_t *yr = y + (int64_t)m * ldy;
+        float amax = 0.0f;
+        for (int k = 0; k < K; ++k) {
+            float sum = oracle_bf16_to_f32(hr[k]) + oracle_bf16_to_f32(yr[k]);
+            t[k] = oracle_f32_to_bf16_rne(sum);
+            float a = fabsf(oracle_bf16_to_f32(t[k]));
+            if (a > amax) amax = a;
+        }
+        int e = (amax == 0.0f) ? 0 : ilogbf(amax);
+        for (int k = 0; k < K; ++k) {
+            double scaled = ldexp((double)oracle_bf16_to_f32(t[k]), -e);
+            hr[k] = oracle_f32_to_bf16_rne((float)scaled);
+        }
+    }
+    free(t);
+}
+
+/*
+ * MLP product: out[m, k] = bf16_rne(relu(g) * u) with g = gu[m, k] and
+ * u = gu[m, K + k] (the gate and up halves of one packed gate/up output, row
+ * stride ld >= 2K), relu(g) = g if g > 0 else +0, the product one fp32
+ * multiply (exact for two bf16 values in the normal range).
+ */
+void oracle_relu_mul(const uint16_t *gu, int64_t ld, int M, int K, uint16_t *out)
+{
+    for (int m = 0; m < M; ++m) {
+        const uint16_t *r = gu + (int64_t)m * ld;
+        for (int k = 0; k < K; ++k) {
+            float g = oracle_bf16_to_f32(r[k]);
+            float u = oracle_bf16_to_f32(r[K + k]);
+            float gr = (g > 0.0f) ? g : 0.0f;
+            out[(int64_t)m * K + k] = oracle_f32_to_bf16_rne(gr * u);
+        }
+    }
+}
+
 /* Number of OpenMP threads the parallel loops above use (1 without OpenMP). */
 int oracle_num_threads(void)
 {

@@ -102,3 +102,72 @@ def nearest_pow2_log(s: float) -> float:
         if best is None or d < best[0]:
             best = (d, j)
     return 2.0 ** best[1]
+
+
+def _is_neg_zero_bits(b: int) -> bool:
+    return (int(b) & 0xFFFF) == 0x8000
+
+
+def _bits_of(v: Fraction, neg_zero: bool) -> int:
+    if v == 0:
+        return 0x8000 if neg_zero else 0x0000
+    return bf16_bits(v)
+
+
+def residual_rescale_row(h_bits, y_bits):
+    """Exact restatement of the residual step on one row of bf16 patterns.
+
+    t = bf16 of the exact sum h + y (one rounding); e = floor(log2 max|t|)
+    (0 for an all-zero row); result = bf16 of the exact t * 2^-e.  Signed
+    zeros follow IEEE: an exact-zero sum is +0 unless both addends are -0; a
+    nonzero value that rounds to zero keeps its sign."""
+    t = []
+    for hb, yb in zip(h_bits, y_bits):
+        hv, yv = bf16_value(hb), bf16_value(yb)
+        s = hv + yv
+        if s == 0:
+            t.append((Fraction(0), _is_neg_zero_bits(hb) and _is_neg_zero_bits(yb)))
+        else:
+            r = rn_bf16(s)
+            t.append((r, r == 0 and s < 0))
+    amax = max(abs(v) for v, _ in t)
+    if amax == 0:
+        e = 0
+    else:
+        e = amax.numerator.bit_length() - amax.denominator.bit_length()
+        if Fraction(2) ** e > amax:
+            e -= 1
+    out = []
+    for v, nz in t:
+        if v == 0:
+            out.append(_bits_of(Fraction(0), nz))
+            continue
+        r = rn_bf16(v * Fraction(2) ** (-e))
+        out.append(_bits_of(r, v < 0))
+    return out
+
+
+def relu_mul_row(g_bits, u_bits):
+    """bf16 of the exact relu(g) * u per element (relu(g) = g if g > 0 else +0)."""
+    out = []
+    for gb, ub in zip(g_bits, u_bits):
+        g, u = bf16_value(gb), bf16_value(ub)
+        u_neg = (int(ub) & 0x8000) != 0
+        gr = g if g > 0 else Fraction(0)
+        p = gr * u
+        if p == 0:
+            out.append(0x8000 if u_neg else 0x0000)   # +0 * u carries u's sign
+            continue
+        r = rn_bf16(p)
+        out.append(_bits_of(r, p < 0))
+    return out
+
+
+def argmax_bf16(row_bits):
+    """Lowest index of the largest bf16 value (-0 == +0)."""
+    best, bv = 0, bf16_value(row_bits[0])
+    for n in range(1, len(row_bits)):
+        v = bf16_value(row_bits[n])
+        if v > bv:
+            best, bv = n, v
+    return best

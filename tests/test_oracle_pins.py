@@ -438,3 +438,145 @@ def test_lmhead_near_tie_workload_structure():
         va, vb = gen.bf16_bits_to_f32(logits[m, [a, b]])
         assert abs(float(va) - float(vb)) <= 0.25
         assert am[m] in (a, b)
+
+
+# --------------------------------------------------------------- chained pass
+
+def _crafted_rows(K):
+    """Rows of (h, y) bf16 patterns that reach the edge cases of the residual step."""
+    rng = np.random.default_rng(77)
+    rows = []
+    h = gen.act_bf16(61, 1, 1, K)[0]
+    y = gen.act_bf16(62, 1, 1, K, sigma=0.3)[0]
+    rows.append((h, y))                                          # ordinary
+    rows.append((np.zeros(K, np.uint16), np.zeros(K, np.uint16)))  # all +0: e = 0
+    nz = np.full(K, 0x8000, np.uint16)
+    rows.append((nz, nz.copy()))                                 # -0 + -0 stays -0
+    rows.append((h, h ^ 0x8000))                                 # exact cancellation: +0
+    tiny = np.array([bf16_pattern(v) for v in rng.choice([2.0 ** -130, -(2.0 ** -131), 3 * 2.0 ** -133, 0.0], K)],
+                    np.uint16)
+    rows.append((tiny, np.zeros(K, np.uint16)))                  # subnormal absmax: scale up by 2^130
+    big = np.array([bf16_pattern(v) for v in rng.choice([2.0 ** 100, -3 * 2.0 ** 90, 2.0 ** -30, 1.5], K)],
+                   np.uint16)
+    rows.append((big, h))                                        # large values: scale down
+    ones = np.full(K, bf16_pattern(1.0), np.uint16)
+    ties = np.array([bf16_pattern(v) for v in rng.choice([2.0 ** -8, 3 * 2.0 ** -8, -(2.0 ** -9), 2.0 ** -7], K)],
+                    np.uint16)
+    rows.append((ones, ties))                                    # sums on bf16 ties
+    mixed = np.array([bf16_pattern(v) for v in rng.choice([2.0 ** 100, 2.0 ** -30, -(2.0 ** -33), 3 * 2.0 ** -40,
+                                                           -(2.0 ** -126), 255 * 2.0 ** -40], K)], np.uint16)
+    rows.append((mixed, np.zeros(K, np.uint16)))                 # rescale pushes elements under the normal range
+    return rows
+
+
+def test_residual_rescale_against_exact_rational():
+    K = 48
+    rows = _crafted_rows(K)
+    h = np.stack([r[0] for r in rows])
+    y = np.stack([r[1] for r in rows])
+    got = oracle.residual_rescale(h, y)
+    for i in range(len(rows)):
+        assert got[i].tolist() == ex.residual_rescale_row(h[i].tolist(), y[i].tolist()), i
+
+
+def test_residual_rescale_row_stride_and_range():
+    """y may be wider than h (its first K columns are added); a nonzero row ends
+    with absmax in [1, 2), and the codes of per-row quantisation do not change."""
+    M, K = 6, 256
+    h = gen.act_bf16(63, 1, M, K, outliers=gen.outlier_channels(63, K), gain=20.0)
+    y = gen.act_bf16(64, 1, M, 3 * K, sigma=4.0)
+    got = oracle.residual_rescale(h, y)
+    for m in range(M):
+        assert got[m].tolist() == ex.residual_rescale_row(h[m].tolist(), y[m, :K].tolist())
+        vals = gen.bf16_bits_to_f32(got[m])
+        assert 1.0 <= np.abs(vals).max() < 2.0
+        t = np.array(ex.residual_rescale_row(h[m].tolist(), y[m, :K].tolist()), np.uint16)
+        # quantisation of the unscaled sum gives the same codes as of the rescaled row
+        unscaled = oracle.f32_to_bf16_rne_array(gen.bf16_bits_to_f32(h[m]) + gen.bf16_bits_to_f32(y[m, :K]))
+        qa, _ = oracle.quantize_act(unscaled[None, :])
+        qb, _ = oracle.quantize_act(t[None, :])
+        assert np.array_equal(qa, qb)
+
+
+def test_relu_mul_against_exact_rational():
+    rng = np.random.default_rng(78)
+    M, K = 4, 40
+    gu = gen.act_bf16(65, 1, M, 2 * K + 8, sigma=2.0)
+    # signed zeros, negative gates, tiny products that leave the normal range
+    special = [0.0, -0.0, -1.5, 2.0 ** -70, -(2.0 ** -70), 2.0 ** -66, 3.0, 2.0 ** 60]
+    gu[0, :K] = [bf16_pattern(v) for v in rng.choice(special, K)]
+    gu[0, K:2 * K] = [bf16_pattern(v) for v in rng.choice(special, K)]
+    got = oracle.relu_mul(gu, K)
+    for m in range(M):
+        assert got[m].tolist() == ex.relu_mul_row(gu[m, :K].tolist(), gu[m, K:2 * K].tolist()), m
+
+
+def _tiny_stack(seed, H=32, I=48, QR=32, KV=16, V=64, layers=2):
+    def wq(layer, proj, N, K):
+        q, s = oracle.quantize_weight(gen.weight_f32(seed, layer, proj, N, K))
+        return oracle.requant_pow2(q, s)
+    Ls = []
+    for l in range(layers):
+        Ls.append({"qkv": wq(l, 0, QR + 2 * KV, H), "o": wq(l, 3, H, QR),
+                   "gu": wq(l, 4, 2 * I, H), "down": wq(l, 6, H, I)})
+    head = wq(99, 0, V, H)
+    return Ls, head, QR
+
+
+def _exact_lin(q_rows, s_a, wq, s_w):
+    return ex.linear(q_rows, [Fraction(float(v)) for v in s_a], wq.tolist(), [Fraction(float(v)) for v in s_w])
+
+
+def _exact_quant(bits_rows):
+    out_q, out_s = [], []
+    for row in bits_rows:
+        c, s = ex.quantize_row([ex.bf16_value(b) for b in row])
+        out_q.append(c)
+        out_s.append(s)
+    return out_q, out_s
+
+
+def test_verify_pass_tiny_against_exact_rational():
+    """Two chained layers and the head, every step recomputed with exact rationals."""
+    Ls, head, QR = _tiny_stack(5)
+    M = 3
+    h0 = gen.act_bf16(66, 1, M, 32, outliers=gen.outlier_channels(66, 32, 2), gain=20.0)
+    am, h_end, recs = oracle.verify_pass(h0, Ls, head, QR, record=True)
+
+    def lin(bits_rows, w):
+        q, s = _exact_quant(bits_rows)
+        return ex.linear(q, s, w[0].tolist(), [Fraction(float(v)) for v in w[1]])
+
+    h = h0.tolist()
+    for L, rec in zip(Ls, recs):
+        y_qkv = lin(h, L["qkv"])
+        assert rec["qkv"].tolist() == y_qkv
+        y_o = lin([r[:QR] for r in y_qkv], L["o"])
+        assert rec["o"].tolist() == y_o
+        h = [ex.residual_rescale_row(hr, yr) for hr, yr in zip(h, y_o)]
+        assert rec["h_mid"].tolist() == h
+        y_gu = lin(h, L["gu"])
+        assert rec["gu"].tolist() == y_gu
+        inter = len(y_gu[0]) // 2
+        m = [ex.relu_mul_row(r[:inter], r[inter:]) for r in y_gu]
+        y_d = lin(m, L["down"])
+        assert rec["down"].tolist() == y_d
+        h = [ex.residual_rescale_row(hr, yr) for hr, yr in zip(h, y_d)]
+        assert rec["h"].tolist() == h
+    logits = lin(h, head)
+    assert am.tolist() == [ex.argmax_bf16(r) for r in logits]
+    assert h_end.tolist() == h
+
+
+def test_verify_pass_rows_are_batch_invariant():
+    """Each row of a 5-row chained pass equals the 1-row pass on that row alone,
+    layer by layer."""
+    Ls, head, QR = _tiny_stack(6, H=64, I=96, QR=64, KV=32, V=256, layers=3)
+    h0 = gen.act_bf16(67, 1, 5, 64, outliers=gen.outlier_channels(67, 64), gain=20.0)
+    am, h_end, recs = oracle.verify_pass(h0, Ls, head, QR, record=True)
+    for r in range(5):
+        am1, h1, recs1 = oracle.verify_pass(h0[r:r + 1], Ls, head, QR, record=True)
+        assert am1[0] == am[r] and np.array_equal(h1[0], h_end[r])
+        for a, b in zip(recs, recs1):
+            for k in a:
+                assert np.array_equal(a[k][r], b[k][0]), k
