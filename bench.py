@@ -1,21 +1,26 @@
 #!/usr/bin/env python3
-"""Benchmark: one verify pass of a 36-layer Qwen3-8B-shaped W8A8 stack.
+"""Benchmark: one chained verify pass of a 36-layer Qwen3-8B-shaped W8A8 stack.
 
-A step is one pass of the whole hot path over one batch of M tokens: for each
-of 36 layers, per-token activation quantisation of each linear's input and the
-seven linears (q, k, v, o, gate, up, down), then quantisation of the head input
-and the LM head with its greedy argmax.  Weights (7,568,097,280 bytes of int8,
-power-of-two scales) are generated from the seeded recipe, quantised on the
-GPU, and stay resident; the step reads all of them, which is far more than the
-L2 cache, so no explicit flush is needed.  Each linear gets its own synthetic
-bf16 activations (layers are not chained).
+A step is one pass of the whole hot path over one batch of M tokens: the
+residual stream h (bf16 [M, 4096]) runs through 36 layers, each
+    y_qkv = linear(quant(h), W_qkv)          q, k, v packed (6144 rows)
+    y_o   = linear(quant(y_qkv[:, :4096]), W_o)   (q slice: attention stand-in)
+    h     = rescale(bf16(h + y_o));  y_gu = linear(quant(h), W_gu)   gate, up packed
+    y_d   = linear(quant(bf16(relu(gate) * up)), W_down)
+    h     = rescale(bf16(h + y_d))
+and then the LM head's greedy argmax over 151,936 rows.  Every quantisation is
+fused with the elementwise step before it.  Weights (7,568,097,280 bytes of
+int8 plus power-of-two scales) come from the seeded recipe, are quantised on
+the GPU and stay resident; the step reads all of them, far more than the L2
+cache, so no explicit flush is needed.
 
 `value` is weight GB/s over the step (weight codes + scales / step time) with
-the step captured as a CUDA graph; `e2e` is the same metric measured through
-the C-ABI entry points with the step's activations copied from pinned host
-memory and the argmax copied back inside the timed region.
+the step in a CUDA graph; `e2e` is the same metric with the step's input rows
+copied from pinned host memory and the argmax copied back inside the timed
+region.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--m M] [--impl reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--m M] [--mode program|calls]
+    python bench.py --impl reference     # the CPU oracle on a bounded sample
 
 Under torchrun (N > 1) each rank runs an independent replica on its own GPU.
 """
@@ -38,7 +43,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "W8A8 verify-pass linear weight GB/s & % of HBM roofline at M=1–8, bit-exact"
 UNIT = "GB/s"
-WORKLOAD = "qwen3_8b_stack36_verify_pass"
+WORKLOAD = "qwen3_8b_stack36_chained_verify_pass"
 
 # DRAM traffic of the weight-streaming kernel from one ncu capture (bytes read +
 # written per launch, scaled to the given launch) and the hash of the kernel
@@ -144,143 +149,152 @@ class ClockSampler:
 # ------------------------------------------------------------------- model
 
 class Stack:
-    """Resident int8 weights of the stack and per-step activation buffers."""
+    """Resident int8 weights of the chained stack and the pass's buffers
+    (sized for up to 16 tokens; a pass over M tokens uses the first M rows)."""
 
-    def __init__(self, bi, torch, layers: int, M: int, device):
+    H, QR, KV, I, V = 4096, 4096, 1024, 12288, 151936
+    MAXM = 16
+
+    def __init__(self, bi, torch, layers: int, device):
         import gen
-        self.bi, self.torch, self.M, self.dev = bi, torch, M, device
-        self.layers = layers
+        self.bi, self.torch, self.dev, self.layers = bi, torch, device, layers
         wl = gen.STACK36
-        self.lin = gen.QWEN3_8B_LINEARS
-        # Per layer, q/k/v share one input and so do gate/up: their weight
-        # rows are stored back to back ("packed") and each group is one call.
-        # Rows are independent, so the outputs are the same bits as separate
-        # calls.
-        self.groups = [("qkv", ("q", "k", "v"), 4096), ("o", ("o",), 4096), ("gu", ("gate", "up"), 4096),
-                       ("down", ("down",), 12288)]
-        byname = {l.name: l for l in self.lin}
-        self.W = []       # per layer: dict group -> (wq, sw) with the group's rows packed
+        lins = {l.name: l for l in gen.QWEN3_8B_LINEARS}
         self.chunk = 8192
-        self.stage = torch.empty(self.chunk * 12288, dtype=torch.float32).pin_memory()
+        self.stage = torch.empty(self.chunk * self.I, dtype=torch.float32).pin_memory()
         stage_np = self.stage.numpy()
+        self.W = []        # per layer: group -> (wq, sw), member rows packed in order
+        self.weight_bytes = 0
         for l in range(layers):
             d = {}
-            for gname, members, K in self.groups:
-                parts = [self._make_weight(lambda r0, r, lin=byname[m], l=l: gen.weight_f32(
-                    wl.seed, l, lin.proj, lin.N, lin.K, row0=r0, rows=r, out=stage_np), byname[m].N, K)
-                    for m in members]
-                if len(parts) == 1:
-                    d[gname] = parts[0]
-                else:
-                    d[gname] = (torch.cat([p[0] for p in parts]), torch.cat([p[1] for p in parts]))
-                    del parts
+            for gname, members in gen.CHAIN_GROUPS:
+                mats = [lins[m] for m in members]
+                K = mats[0].K
+                N = sum(m.N for m in mats)
+                wq = torch.empty((N, K), dtype=torch.int8, device=device)
+                sw = torch.empty(N, dtype=torch.float32, device=device)
+                off = 0
+                for m in mats:
+                    self._quantise_rows(lambda r0, r, m=m, l=l: gen.weight_f32(
+                        wl.seed, l, m.proj, m.N, m.K, row0=r0, rows=r, out=stage_np), m.N, K,
+                        wq[off:off + m.N], sw[off:off + m.N])
+                    off += m.N
+                d[gname] = (wq, sw)
+                self.weight_bytes += N * K + 4 * N
             self.W.append(d)
-        # LM head with the planted near-tie rows for the head's activation rows
-        self.x_head_np = gen.activations(wl, 16, gen.LMHEAD.K, stream=7)
-        xh = self.x_head_np[:8]
-        self.head = self._make_weight(lambda r0, r: gen.lmhead_weight_f32(wl.seed, xh, r0, r, out=stage_np),
-                                      gen.LMHEAD.N, gen.LMHEAD.K)
+        hq = torch.empty((self.V, self.H), dtype=torch.int8, device=device)
+        hs = torch.empty(self.V, dtype=torch.float32, device=device)
+        self._quantise_rows(lambda r0, r: gen.weight_f32(wl.seed, 0, gen.LMHEAD.proj, self.V, self.H, row0=r0,
+                                                         rows=r, out=stage_np), self.V, self.H, hq, hs)
+        self.head = (hq, hs)
+        self.weight_bytes += self.V * self.H + 4 * self.V
         del self.stage
-        self.weight_bytes = sum(l.N * l.K + 4 * l.N for l in self.lin) * layers + \
-            gen.LMHEAD.N * gen.LMHEAD.K + 4 * gen.LMHEAD.N
-        # activations: inputs of q/k/v, o, gate/up, down per layer, and the head
-        self.in_dims = [(g, K) for g, _, K in self.groups]
-        self.x_np = {}
-        self.x = {}
-        for l in range(layers):
-            for j, (nm, K) in enumerate(self.in_dims):
-                a = gen.activations(wl, 16, K, stream=100 + 4 * l + j)
-                self.x_np[(l, nm)] = a
-                self.x[(l, nm)] = torch.from_numpy(a.view(np.int16)).to(device)
-        self.x[("head",)] = torch.from_numpy(self.x_head_np.view(np.int16)).to(device)
-        self.x_np[("head",)] = self.x_head_np
-        self.ws = bi.new_workspace(16, 151936, 12288, device=device)
-        self.q = torch.empty((16, 12288), dtype=torch.int8, device=device)
-        self.s = torch.empty(16, dtype=torch.float32, device=device)
-        self.y = {g: torch.empty((16, self.W[0][g][0].shape[0]), dtype=torch.int16, device=device)
-                  for g, _, _ in self.groups}
-        self.argmax = torch.empty(16, dtype=torch.int32, device=device)
+        # the pass's input rows and buffers
+        self.h0_np = gen.activations(wl, self.MAXM, self.H)
+        t, M16 = torch, self.MAXM
+        self.h0 = t.from_numpy(self.h0_np.view(np.int16)).to(device)
+        self.h = t.empty((M16, self.H), dtype=t.int16, device=device)
+        self.y, self.q, self.s = {}, {}, {}
+        for name, N, K in (("qkv", self.QR + 2 * self.KV, self.H), ("o", self.H, self.QR),
+                           ("gu", 2 * self.I, self.H), ("down", self.H, self.I), ("head", 0, self.H)):
+            if N:
+                self.y[name] = t.zeros((M16, N), dtype=t.int16, device=device)
+            self.q[name] = t.empty((M16, K), dtype=t.int8, device=device)
+            self.s[name] = t.empty(M16, dtype=t.float32, device=device)
+        self.argmax = t.empty(M16, dtype=t.int32, device=device)
+        self.ws = bi.new_workspace(M16, self.V, self.I, device=device)
         torch.cuda.synchronize()
 
-    def _make_weight(self, rows_fn, N, K):
+    def _quantise_rows(self, rows_fn, N, K, wq, sw):
+        """Generate fp32 rows chunk by chunk into pinned memory and quantise
+        them on the GPU (absmax, then power-of-two requantisation)."""
         torch, bi = self.torch, self.bi
-        wq = torch.empty((N, K), dtype=torch.int8, device=self.dev)
-        sw = torch.empty(N, dtype=torch.float32, device=self.dev)
         for r0 in range(0, N, self.chunk):
             r = min(self.chunk, N - r0)
-            rows_fn(r0, r)                      # fills the pinned staging buffer
+            rows_fn(r0, r)
             w = self.stage[:r * K].view(r, K).to(self.dev, non_blocking=True)
             bi.bi_quantize_weight(w, wq[r0:r0 + r], sw[r0:r0 + r])
             bi.bi_requant_pow2(wq[r0:r0 + r], sw[r0:r0 + r], wq[r0:r0 + r], sw[r0:r0 + r])
             torch.cuda.synchronize()
-        return wq, sw
+
+    def ops(self, M):
+        """The pass as executor ops, in order."""
+        bi, y, q, s = self.bi, self.y, self.q, self.s
+        h = self.h[:M]
+        ops = [bi.op_quantize_act(h, q["qkv"][:M], s["qkv"][:M])]
+        for l, W in enumerate(self.W):
+            nxt = "head" if l == self.layers - 1 else "qkv"
+            ops += [bi.op_linear(q["qkv"][:M], s["qkv"][:M], *W["qkv"], y["qkv"][:M]),
+                    bi.op_quantize_act(y["qkv"][:M], q["o"][:M], s["o"][:M], K=self.QR),
+                    bi.op_linear(q["o"][:M], s["o"][:M], *W["o"], y["o"][:M]),
+                    bi.op_residual_quant(h, y["o"][:M], q["gu"][:M], s["gu"][:M]),
+                    bi.op_linear(q["gu"][:M], s["gu"][:M], *W["gu"], y["gu"][:M]),
+                    bi.op_relu_mul_quant(y["gu"][:M], self.I, q["down"][:M], s["down"][:M]),
+                    bi.op_linear(q["down"][:M], s["down"][:M], *W["down"], y["down"][:M]),
+                    bi.op_residual_quant(h, y["down"][:M], q[nxt][:M], s[nxt][:M])]
+        ops.append(bi.op_lmhead(q["head"][:M], s["head"][:M], *self.head, None, self.argmax[:M]))
+        return ops
 
     def build_program(self, M):
-        """The step as one verify-pass program (bi_program_*): the same ops,
-        in the same order, each starting after all earlier ones."""
         bi = self.bi
-        ops = []
-        s = self.s[:M]
-        for l in range(self.layers):
-            for nm, K in self.in_dims:
-                qbuf = self.q.view(-1)[:M * K].view(M, K)
-                ops.append(bi.op_quantize_act(self.x[(l, nm)][:M, :K], qbuf, s, K=K))
-                wq, sw = self.W[l][nm]
-                ops.append(bi.op_linear(qbuf, s, wq, sw, self.y[nm][:M]))
-        K = 4096
-        qbuf = self.q.view(-1)[:M * K].view(M, K)
-        ops.append(bi.op_quantize_act(self.x[("head",)][:M], qbuf, s, K=K))
-        wq, sw = self.head
-        ops.append(bi.op_lmhead(qbuf, s, wq, sw, None, self.argmax[:M]))
+        ops = self.ops(M)
         prog = bi.new_program(len(ops), device=self.dev)
         bi.bi_program_build(ops, prog)
         return prog
 
-    def launches_per_step(self, mode="calls"):
-        if mode == "program":
-            return 1
-        return self.layers * 2 * len(self.groups) + 2
+    def reset(self, M):
+        """Start the pass from the input rows (a device copy, part of the step)."""
+        self.h[:M].copy_(self.h0[:M])
 
-    def linear_bytes(self, M):
-        """Algorithmic bytes of the step's linear launches: W + s_w + q + s_a + y."""
-        tot = 0
-        for l in range(self.layers):
-            for nm, K in self.in_dims:
-                N = self.W[l][nm][0].shape[0]
-                tot += N * K + 4 * N + M * K + 4 * M + 2 * M * N
-        return tot
+    def step_calls(self, M, flags, linears_only=False):
+        """The same pass as one library call per op (or just its linears)."""
+        bi, y, q, s, ws = self.bi, self.y, self.q, self.s, self.ws
+        h = self.h[:M]
+        if not linears_only:
+            bi.bi_quantize_act(h, q["qkv"][:M], s["qkv"][:M], flags=flags)
+        for l, W in enumerate(self.W):
+            nxt = "head" if l == self.layers - 1 else "qkv"
+            bi.bi_linear_w8a8(q["qkv"][:M], s["qkv"][:M], *W["qkv"], y["qkv"][:M], ws, flags=flags)
+            if not linears_only:
+                bi.bi_quantize_act(y["qkv"][:M], q["o"][:M], s["o"][:M], K=self.QR, flags=flags)
+            bi.bi_linear_w8a8(q["o"][:M], s["o"][:M], *W["o"], y["o"][:M], ws, flags=flags)
+            if not linears_only:
+                bi.bi_residual_quantize(h, y["o"][:M], q["gu"][:M], s["gu"][:M], flags=flags)
+            bi.bi_linear_w8a8(q["gu"][:M], s["gu"][:M], *W["gu"], y["gu"][:M], ws, flags=flags)
+            if not linears_only:
+                bi.bi_relu_mul_quantize(y["gu"][:M], self.I, q["down"][:M], s["down"][:M], flags=flags)
+            bi.bi_linear_w8a8(q["down"][:M], s["down"][:M], *W["down"], y["down"][:M], ws, flags=flags)
+            if not linears_only:
+                bi.bi_residual_quantize(h, y["down"][:M], q[nxt][:M], s[nxt][:M], flags=flags)
+        if not linears_only:
+            bi.bi_lmhead_argmax(q["head"][:M], s["head"][:M], *self.head, None, self.argmax[:M], ws,
+                                flags=flags)
+
+    def launches_per_step(self, mode):
+        return 1 if mode == "program" else 2 + 8 * self.layers
+
+    def op_bytes(self, op):
+        """Algorithmic bytes of one op: what it must read and write."""
+        bi = self.bi
+        M, N, K = op.M, op.N, op.K
+        if op.kind == bi.BI_OP_QUANTIZE_ACT:
+            return 2 * M * K + M * K + 4 * M
+        if op.kind == bi.BI_OP_RESIDUAL_QUANT:
+            return 3 * 2 * M * K + M * K + 4 * M
+        if op.kind == bi.BI_OP_RELU_MUL_QUANT:
+            return 2 * 2 * M * K + M * K + 4 * M + (2 * M * K if op.y else 0)
+        tot = N * K + 4 * N + M * K + 4 * M
+        if op.kind == bi.BI_OP_LINEAR:
+            return tot + 2 * M * N
+        return tot + 4 * M + (2 * M * N if op.y else 0)
 
     def step_bytes(self, M):
-        """Algorithmic bytes of one step: every linear's W + s_w + q + s_a + y,
-        every quantisation's x read and q + s_a written, the head's W + s_w +
-        q + s_a and argmax."""
-        tot = self.linear_bytes(M)
-        for l in range(self.layers):
-            for nm, K in self.in_dims:
-                tot += 2 * M * K + M * K + 4 * M
-        N, K = self.head[0].shape
-        tot += 2 * M * K + M * K + 4 * M
-        tot += N * K + 4 * N + M * K + 4 * M + 4 * M
-        return tot
+        """Algorithmic bytes of one step: the input copy and every op."""
+        return 4 * M * self.H + sum(self.op_bytes(o) for o in self.ops(M))
 
-    def step(self, M, flags, linears_only=False):
-        """Enqueue one verify pass on the current stream (or, with
-        linears_only, just its linear launches back to back)."""
-        bi, q, s = self.bi, self.q[:M], self.s[:M]
-        for l in range(self.layers):
-            for nm, K in self.in_dims:
-                qbuf = self.q.view(-1)[:M * K].view(M, K)
-                if not linears_only:
-                    bi.bi_quantize_act(self.x[(l, nm)][:M, :K], qbuf, s, K=K, flags=flags)
-                wq, sw = self.W[l][nm]
-                bi.bi_linear_w8a8(qbuf, s, wq, sw, self.y[nm][:M], self.ws, flags=flags)
-        if linears_only:
-            return
-        K = 4096
-        qbuf = self.q.view(-1)[:M * K].view(M, K)
-        bi.bi_quantize_act(self.x[("head",)][:M], qbuf, s, K=K, flags=flags)
-        wq, sw = self.head
-        bi.bi_lmhead_argmax(qbuf, s, wq, sw, None, self.argmax[:M], self.ws, flags=flags)
+    def linear_bytes(self, M):
+        bi = self.bi
+        return sum(self.op_bytes(o) for o in self.ops(M) if o.kind == bi.BI_OP_LINEAR)
 
 
 def source_sha(path):
@@ -301,7 +315,7 @@ def run_ours(args):
     M = args.m
     assert 1 <= M <= 16
     t0 = time.time()
-    st = Stack(bi, torch, args.layers, 16, dev)
+    st = Stack(bi, torch, args.layers, dev)
     setup_s = time.time() - t0
     flags = bi.BI_FLAG_PDL
     stream = torch.cuda.Stream(device=dev)
@@ -316,12 +330,13 @@ def run_ours(args):
     prog_ws = torch.zeros(bi.bi_program_workspace_size(), dtype=torch.uint8, device=dev)
 
     def enqueue_step(m):
+        st.reset(m)
         if args.mode == "program":
             if m not in progs:
                 progs[m] = st.build_program(m)
             bi.bi_program_run(progs[m], m, prog_ws)
         else:
-            st.step(m, flags)
+            st.step_calls(m, flags)
 
     def graph_for(m):
         with torch.cuda.stream(stream):
@@ -385,22 +400,22 @@ def run_ours(args):
         # back to back in a CUDA graph (same launch configuration as the step),
         # timed with events on the launching stream
         with torch.cuda.stream(stream):
-            st.step(M, flags, linears_only=True)
+            st.step_calls(M, flags, linears_only=True)
         stream.synchronize()
         gl = torch.cuda.CUDAGraph()
         with torch.cuda.graph(gl, stream=stream):
-            st.step(M, flags, linears_only=True)
+            st.step_calls(M, flags, linears_only=True)
         kernel_name = "skinny_kernel (bi_linear_w8a8, M<=16)"
-        lin_launches = st.layers * len(st.groups)
+        lin_launches = st.layers * 4
         lin_ms = time_graph(gl, max(5, args.steps // 2), 3)
         achieved = st.linear_bytes(M) / (lin_ms * 1e-3) / 1e9
         note = ("achieved = algorithmic bytes (W + s_w + q + s_a + y) of the step's %d linear launches / "
                 "their event-timed duration back to back in a CUDA graph" % lin_launches)
 
-    # end to end: activations H2D from pinned memory, graph, argmax D2H
-    host_x = {k: torch.from_numpy(v.view(np.int16)).pin_memory() for k, v in st.x_np.items()}
+    # end to end: the input rows H2D from pinned memory, the step's graph, argmax D2H
+    host_h0 = torch.from_numpy(st.h0_np.view(np.int16)).pin_memory()
     host_am = torch.empty(16, dtype=torch.int32).pin_memory()
-    h2d = sum(int(v[:M].numel()) * 2 for v in host_x.values())
+    h2d = int(host_h0[:M].numel()) * 2
     e2e_steps = max(3, args.steps // 2)
     barrier()
     e0 = torch.cuda.Event(enable_timing=True)
@@ -408,8 +423,7 @@ def run_ours(args):
     with torch.cuda.stream(stream):
         e0.record(stream)
         for _ in range(e2e_steps):
-            for k, v in host_x.items():
-                st.x[k][:M].copy_(v[:M], non_blocking=True)
+            st.h0[:M].copy_(host_h0[:M], non_blocking=True)
             g.replay()
             host_am[:M].copy_(st.argmax[:M], non_blocking=True)
         e1.record(stream)
@@ -436,10 +450,12 @@ def run_ours(args):
             "config": {"workload": WORKLOAD, "M": M, "layers": args.layers, "hidden": 4096,
                        "intermediate": 12288, "vocab": 151936, "weight_bytes_per_step": st.weight_bytes,
                        "l2": "inputs larger than L2 (all weights read once per step)",
-                       "activations": "independent synthetic input per linear group (layers not chained)",
+                       "activations": ("chained: residual stream through 36 layers (q slice of q/k/v as the "
+                                       "attention stand-in, ReLU-gated MLP, power-of-two row rescale)"),
                        "packing": "q/k/v and gate/up weight rows packed: one call per group",
                        "launch": ("one verify-pass program launch per step (persistent cooperative kernel, "
-                                  "grid barrier between ops), in a CUDA graph" if args.mode == "program" else
+                                  "grid barrier between ops) after a device copy of the input rows, in a CUDA "
+                                  "graph" if args.mode == "program" else
                                   "CUDA graph of the step, one launch per op, programmatic dependent launch"),
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "pct_of_hbm_copy": round(100 * gbs / world / peak, 1),
@@ -466,56 +482,64 @@ def run_ours(args):
 # ------------------------------------------------------------------ CPU oracle
 
 def oracle_sample():
-    """A bounded sample of the workload for the CPU oracle: layer 0's q
-    projection (4096 x 4096) at M = 8, weights quantised by the oracle."""
+    """A bounded sample of the workload for the CPU oracle: layer 0 of the
+    chained stack (all four packed linears and the fused elementwise steps),
+    weights generated from the same recipe and quantised by the oracle."""
     import gen
     import oracle
     wl = gen.STACK36
-    lin = gen.QWEN3_8B_LINEARS[0]
-    w = gen.weight_f32(wl.seed, 0, lin.proj, lin.N, lin.K)
-    wq, sw = oracle.requant_pow2(*oracle.quantize_weight(w))
-    x = gen.activations(wl, 8, lin.K, stream=100)
-    return oracle, x, wq, sw, lin
+    L = {}
+    for gname, _ in gen.CHAIN_GROUPS:
+        w = gen.chain_group_f32(wl.seed, 0, gname)
+        L[gname] = oracle.requant_pow2(*oracle.quantize_weight(w))
+        del w
+    layer_bytes = sum(wq.size + 4 * sw.size for wq, sw in L.values())
+    h0 = gen.activations(wl, Stack.MAXM, Stack.H)
+    return oracle, L, h0, layer_bytes
+
+
+def _oracle_layer(oracle, L, h0, M):
+    oracle.chain_layer(h0[:M], L, Stack.QR)
 
 
 def cpu_baseline(bounded_s=12.0, M=8):
-    oracle, x, wq, sw, lin = oracle_sample()
+    oracle, L, h0, layer_bytes = oracle_sample()
     t0 = time.time()
     n = 0
     while True:
-        q, s = oracle.quantize_act(x[:M])
-        oracle.linear_w8a8(q, s, wq, sw)
+        _oracle_layer(oracle, L, h0, M)
         n += 1
         if time.time() - t0 >= bounded_s:
             break
     dt = (time.time() - t0) / n
-    return {"value": round((lin.N * lin.K + 4 * lin.N) / dt / 1e9, 3), "unit": UNIT,
+    return {"value": round(layer_bytes / dt / 1e9, 3), "unit": UNIT,
             "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": "q projection of layer 0 (4096x4096 int8, pow2 scales) at M=%d, activation "
-                      "quantisation + linear, repeated %d times in %.1f s" % (M, n, time.time() - t0)}
+            "sample": "layer 0 of the chained stack (q/k/v, o, gate/up, down with the fused quantisation, "
+                      "residual and MLP steps; %d weight bytes) at M=%d, repeated %d times in %.1f s"
+                      % (layer_bytes, M, n, time.time() - t0)}
 
 
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    oracle, x, wq, sw, lin = oracle_sample()
+    oracle, L, h0, layer_bytes = oracle_sample()
     M = args.m
     for _ in range(args.warmup):
-        q, s = oracle.quantize_act(x[:M])
-        oracle.linear_w8a8(q, s, wq, sw)
+        _oracle_layer(oracle, L, h0, M)
     t0 = time.time()
     for _ in range(args.steps):
-        q, s = oracle.quantize_act(x[:M])
-        oracle.linear_w8a8(q, s, wq, sw)
+        _oracle_layer(oracle, L, h0, M)
     dt = (time.time() - t0) / args.steps
-    v = (lin.N * lin.K + 4 * lin.N) / dt / 1e9
+    v = layer_bytes / dt / 1e9
+    sample = ("one step = layer 0 of the chained stack (%d weight bytes) at M=%d on the CPU oracle"
+              % (layer_bytes, M))
     line = {"impl": "reference", "metric": METRIC, "value": round(v, 3), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8",
             "data": "synthetic", "config": {"workload": WORKLOAD, "M": M},
             "cpu_baseline": {"value": round(v, 3), "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
-                             "sample": "one step = layer 0's 4096x4096 q projection at M=%d on the CPU oracle" % M},
+                             "sample": sample},
             "e2e": {"value": round(v, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 

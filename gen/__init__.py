@@ -139,6 +139,29 @@ INTERMEDIATE = 12288
 N_LAYERS = 36
 
 
+# A layer of the chained verify pass: members that read the same input are
+# stored as one packed weight matrix (rows of the members back to back, in
+# this order), so each group is one linear.
+CHAIN_GROUPS = (("qkv", ("q", "k", "v")), ("o", ("o",)), ("gu", ("gate", "up")), ("down", ("down",)))
+
+
+def chain_linears(H: int, QR: int, KV: int, I: int) -> tuple:
+    """The seven projections of a layer with hidden H, q rows QR, k/v rows KV
+    and intermediate I (Qwen3-8B: 4096, 4096, 1024, 12288), with the weight
+    stream indices of QWEN3_8B_LINEARS."""
+    return (Linear("q", H, QR, 0), Linear("k", H, KV, 1), Linear("v", H, KV, 2), Linear("o", QR, H, 3),
+            Linear("gate", H, I, 4), Linear("up", H, I, 5), Linear("down", I, H, 6))
+
+
+def chain_group_f32(seed: int, layer: int, group: str, linears=QWEN3_8B_LINEARS) -> np.ndarray:
+    """fp32 weights of one packed group of a layer: its members' matrices
+    (each from its own weight stream) stacked in CHAIN_GROUPS order."""
+    byname = {l.name: l for l in linears}
+    members = dict(CHAIN_GROUPS)[group]
+    mats = [weight_f32(seed, layer, byname[m].proj, byname[m].N, byname[m].K) for m in members]
+    return mats[0] if len(mats) == 1 else np.concatenate(mats, axis=0)
+
+
 @dataclass(frozen=True)
 class Workload:
     name: str

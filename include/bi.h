@@ -94,6 +94,42 @@ BI_API bi_status bi_quantize_act(const uint16_t *x, int64_t ldx, int M, int K,
                           int8_t *q, float *s_a, unsigned flags, bi_stream_t stream);
 
 /*
+ * Chained verify pass: the two elementwise steps between a layer's linears,
+ * each fused with the activation quantisation of the linear that reads it.
+ * A decode/verify pass chains its linears through the residual stream ("why
+ * speculative decoding changed my output", "the mat-vec kernel"; "My
+ * speculative decoder got slower", "The physics"); the pages print no layer
+ * body, so the steps are this library's reading, both exact roundings of
+ * fp32 operations on bf16 values (fp32 has enough bits that an fp32 add or
+ * multiply of two bf16 values, then bf16 rounding, equals one rounding of
+ * the exact result):
+ *
+ * bi_residual_quantize: the residual update after the o and down projections.
+ *   h    bf16 [M, K] (row stride K), read and written in place
+ *   y    bf16 [M, ldy], first K columns added (read only; must not overlap h)
+ *   h'   = bf16_rne(h + y)  (fp32 add);  e = floor(log2 max_k |h'[m, k]|),
+ *          0 for an all-zero row;  h = bf16_rne(h' * 2^-e)
+ *   q, s_a = bi_quantize_act of the new h (the power-of-two rescale keeps a
+ *          deep stack finite and changes no code: per-row absmax quantisation
+ *          is exactly invariant to scaling a row by a power of two)
+ *
+ * bi_relu_mul_quantize: the gated MLP product feeding the down projection.
+ *   gu   bf16 [M, ldgu] (ldgu >= 2K): gate g = gu[:, 0:K], up u = gu[:, K:2K]
+ *        (the output of one packed gate/up linear), read only
+ *   m    = bf16_rne(relu(g) * u), relu(g) = g if g > 0 else +0 (fp32 multiply)
+ *   q, s_a = bi_quantize_act of m;  m_out bf16 [M, K] (row stride K) receives
+ *          m unless it is NULL (it must not overlap gu)
+ *
+ * Both: 16-byte aligned h, y, gu, m_out and q; row strides multiples of 8
+ * elements; K % 16 == 0.  One CTA per row; with BI_FLAG_PDL the kernel waits
+ * for the preceding kernel before reading.
+ */
+BI_API bi_status bi_residual_quantize(uint16_t *h, const uint16_t *y, int64_t ldy, int M, int K,
+                                      int8_t *q, float *s_a, unsigned flags, bi_stream_t stream);
+BI_API bi_status bi_relu_mul_quantize(const uint16_t *gu, int64_t ldgu, int M, int K, int8_t *q, float *s_a,
+                                      uint16_t *m_out, unsigned flags, bi_stream_t stream);
+
+/*
  * Checkpoint-style per-output-channel weight quantisation (offline, not part
  * of the verify pass): the same rule as bi_quantize_act applied to each row of
  * an fp32 matrix.
@@ -198,19 +234,24 @@ BI_API bi_status bi_workspace_status(void *ws, size_t ws_bytes, bi_stream_t stre
 typedef enum {
     BI_OP_QUANTIZE_ACT = 1, /* x, ldx, M, K -> q, s_a        (bi_quantize_act)  */
     BI_OP_LINEAR = 2,       /* q, s_a, M, K, w_q, s_w, N -> y (bi_linear_w8a8, M <= 16) */
-    BI_OP_LMHEAD = 3        /* ... -> y (logits, may be NULL), argmax (bi_lmhead_argmax) */
+    BI_OP_LMHEAD = 3,       /* ... -> y (logits, may be NULL), argmax (bi_lmhead_argmax) */
+    BI_OP_RESIDUAL_QUANT = 4, /* y = h [M, K] in/out, x = addend (ldx), M, K -> q, s_a
+                                 (bi_residual_quantize) */
+    BI_OP_RELU_MUL_QUANT = 5  /* x = packed gate|up [M, ldx >= 2K], M, K -> q, s_a,
+                                 y = m or NULL (bi_relu_mul_quantize) */
 } bi_op_kind;
 
 typedef struct {
     int kind;               /* bi_op_kind */
-    int M, N, K;            /* N unused by BI_OP_QUANTIZE_ACT */
-    const uint16_t *x;      /* BI_OP_QUANTIZE_ACT input rows */
+    int M, N, K;            /* N unused by the three quantising kinds */
+    const uint16_t *x;      /* quantising kinds: input rows (see above) */
     int64_t ldx;
     int8_t *q;              /* quantise: output; linear / head: input */
     float *s_a;             /* quantise: output; linear / head: input */
     const int8_t *w_q;      /* linear / head weights [N, K] */
     const float *s_w;       /* [N] */
-    uint16_t *y;            /* linear: output [M, N]; head: logits or NULL */
+    uint16_t *y;            /* linear: output [M, N]; head: logits or NULL;
+                               residual: the stream h; relu-mul: m or NULL */
     int32_t *argmax;        /* head: output [M] */
 } bi_op;
 

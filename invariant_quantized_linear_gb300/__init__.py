@@ -30,6 +30,10 @@ lib.bi_status_string.argtypes = [_ci]
 lib.bi_status_string.restype = ctypes.c_char_p
 lib.bi_quantize_act.argtypes = [_vp, _i64, _ci, _ci, _vp, _vp, _cu, _vp]
 lib.bi_quantize_act.restype = _ci
+lib.bi_residual_quantize.argtypes = [_vp, _vp, _i64, _ci, _ci, _vp, _vp, _cu, _vp]
+lib.bi_residual_quantize.restype = _ci
+lib.bi_relu_mul_quantize.argtypes = [_vp, _i64, _ci, _ci, _vp, _vp, _vp, _cu, _vp]
+lib.bi_relu_mul_quantize.restype = _ci
 lib.bi_quantize_weight.argtypes = [_vp, _i64, _ci, _ci, _vp, _vp, _vp]
 lib.bi_quantize_weight.restype = _ci
 lib.bi_requant_pow2.argtypes = [_vp, _vp, _ci, _ci, _vp, _vp, _vp]
@@ -68,6 +72,8 @@ lib.bi_program_run.restype = _ci
 BI_OP_QUANTIZE_ACT = 1
 BI_OP_LINEAR = 2
 BI_OP_LMHEAD = 3
+BI_OP_RESIDUAL_QUANT = 4
+BI_OP_RELU_MUL_QUANT = 5
 
 BI_OK = 0
 BI_ERR_INVALID_ARG = 1
@@ -112,6 +118,25 @@ def bi_quantize_act(x: torch.Tensor, q: torch.Tensor, s_a: torch.Tensor, K: int 
     K = x.shape[1] if K is None else K
     _check(lib.bi_quantize_act(_ptr(x), x.stride(0), M, K, _ptr(q), _ptr(s_a), flags, _stream(stream)),
            "bi_quantize_act")
+
+
+def bi_residual_quantize(h: torch.Tensor, y: torch.Tensor, q: torch.Tensor, s_a: torch.Tensor,
+                         flags: int = 0, stream=None) -> None:
+    """h: bf16 [M, K] contiguous, updated in place; y: bf16 [M, >= K] (row stride
+    y.stride(0)), first K columns added; q: int8 [M, K]; s_a: fp32 [M]."""
+    M, K = h.shape
+    assert h.stride(0) == K
+    _check(lib.bi_residual_quantize(_ptr(h), _ptr(y), y.stride(0), M, K, _ptr(q), _ptr(s_a), flags,
+                                    _stream(stream)), "bi_residual_quantize")
+
+
+def bi_relu_mul_quantize(gu: torch.Tensor, K: int, q: torch.Tensor, s_a: torch.Tensor,
+                         m_out: torch.Tensor | None = None, flags: int = 0, stream=None) -> None:
+    """gu: bf16 [M, >= 2K] packed gate|up (row stride gu.stride(0)); q: int8 [M, K];
+    s_a: fp32 [M]; m_out: bf16 [M, K] or None."""
+    M = gu.shape[0]
+    _check(lib.bi_relu_mul_quantize(_ptr(gu), gu.stride(0), M, K, _ptr(q), _ptr(s_a), _ptr(m_out), flags,
+                                    _stream(stream)), "bi_relu_mul_quantize")
 
 
 def bi_quantize_weight(w: torch.Tensor, w_q: torch.Tensor, s_w: torch.Tensor, stream=None) -> None:
@@ -189,6 +214,21 @@ def op_quantize_act(x: torch.Tensor, q: torch.Tensor, s_a: torch.Tensor, K: int 
     M = x.shape[0]
     K = x.shape[1] if K is None else K
     return bi_op(BI_OP_QUANTIZE_ACT, M, 0, K, _ptr(x), x.stride(0), _ptr(q), _ptr(s_a), None, None, None, None)
+
+
+def op_residual_quant(h: torch.Tensor, y: torch.Tensor, q: torch.Tensor, s_a: torch.Tensor) -> bi_op:
+    """h (in/out, contiguous [M, K]) <- rescale(bf16(h + y[:, :K])); q, s_a <- quant(h)."""
+    M, K = h.shape
+    assert h.stride(0) == K
+    return bi_op(BI_OP_RESIDUAL_QUANT, M, 0, K, _ptr(y), y.stride(0), _ptr(q), _ptr(s_a), None, None, _ptr(h), None)
+
+
+def op_relu_mul_quant(gu: torch.Tensor, K: int, q: torch.Tensor, s_a: torch.Tensor,
+                      m_out: torch.Tensor | None = None) -> bi_op:
+    """q, s_a <- quant(bf16(relu(gu[:, :K]) * gu[:, K:2K])); m_out receives the product if given."""
+    M = gu.shape[0]
+    return bi_op(BI_OP_RELU_MUL_QUANT, M, 0, K, _ptr(gu), gu.stride(0), _ptr(q), _ptr(s_a), None, None,
+                 _ptr(m_out), None)
 
 
 def op_linear(q: torch.Tensor, s_a: torch.Tensor, w_q: torch.Tensor, s_w: torch.Tensor, y: torch.Tensor) -> bi_op:

@@ -26,6 +26,13 @@ bool aligned4(const void *p)
     return (reinterpret_cast<uintptr_t>(p) & 3u) == 0;
 }
 
+// [a, a + n) and [b, b + m) (bytes) share a byte
+bool overlaps(const void *a, size_t n, const void *b, size_t m)
+{
+    const char *pa = static_cast<const char *>(a), *pb = static_cast<const char *>(b);
+    return pa < pb + m && pb < pa + n;
+}
+
 bi_status from_cuda(cudaError_t e)
 {
     return e == cudaSuccess ? BI_OK : BI_ERR_CUDA;
@@ -162,6 +169,41 @@ bi_status bi_quantize_act(const uint16_t *x, int64_t ldx, int M, int K, int8_t *
     st = device_info(nullptr);
     if (st != BI_OK) return st;
     return from_cuda(bi::launch_quantize_act(x, ldx, M, K, q, s_a, (flags & BI_FLAG_PDL) != 0, stream));
+}
+
+bi_status bi_residual_quantize(uint16_t *h, const uint16_t *y, int64_t ldy, int M, int K, int8_t *q, float *s_a,
+                               unsigned flags, bi_stream_t stream)
+{
+    if (!h || !y || !q || !s_a) return BI_ERR_INVALID_ARG;
+    if (M < 1 || M > 65535 || ldy < K) return BI_ERR_INVALID_ARG;
+    bi_status st = check_k(K);
+    if (st != BI_OK) return st;
+    if (!aligned16(h) || !aligned16(y) || !aligned16(q) || !aligned4(s_a) || (ldy % 8) != 0) return BI_ERR_ALIGNMENT;
+    const size_t hb = static_cast<size_t>(M) * K * 2;
+    const size_t yb = (static_cast<size_t>(M - 1) * ldy + K) * 2;
+    if (overlaps(h, hb, y, yb) || overlaps(h, hb, q, static_cast<size_t>(M) * K) ||
+        overlaps(h, hb, s_a, 4u * M))
+        return BI_ERR_INVALID_ARG;
+    st = device_info(nullptr);
+    if (st != BI_OK) return st;
+    return from_cuda(bi::launch_residual_quantize(h, y, ldy, M, K, q, s_a, (flags & BI_FLAG_PDL) != 0, stream));
+}
+
+bi_status bi_relu_mul_quantize(const uint16_t *gu, int64_t ldgu, int M, int K, int8_t *q, float *s_a,
+                               uint16_t *m_out, unsigned flags, bi_stream_t stream)
+{
+    if (!gu || !q || !s_a) return BI_ERR_INVALID_ARG;
+    if (M < 1 || M > 65535 || ldgu < 2LL * K) return BI_ERR_INVALID_ARG;
+    bi_status st = check_k(K);
+    if (st != BI_OK) return st;
+    if (!aligned16(gu) || !aligned16(q) || !aligned4(s_a) || (ldgu % 8) != 0 || (m_out && !aligned16(m_out)))
+        return BI_ERR_ALIGNMENT;
+    if (m_out && overlaps(m_out, static_cast<size_t>(M) * K * 2, gu, (static_cast<size_t>(M - 1) * ldgu + 2 * K) * 2))
+        return BI_ERR_INVALID_ARG;
+    st = device_info(nullptr);
+    if (st != BI_OK) return st;
+    return from_cuda(
+        bi::launch_relu_mul_quantize(gu, ldgu, M, K, q, s_a, m_out, (flags & BI_FLAG_PDL) != 0, stream));
 }
 
 bi_status bi_quantize_weight(const float *w, int64_t ldw, int N, int K, int8_t *w_q, float *s_w, bi_stream_t stream)

@@ -19,6 +19,7 @@
 #include "bi.h"
 #include "kernels.cuh"
 #include "ptx.cuh"
+#include "row_ops.cuh"
 #include "stream_mma.cuh"
 
 #include <cuda.h>
@@ -195,7 +196,7 @@ __global__ void __launch_bounds__(kThreads, 2) program_kernel(const ProgHeader *
         auto seek = [&](Cursor &k, int from) {   // first unit of the first linear op >= from
             for (k.op = from; k.op < n_ops; ++k.op) {
                 const DevOp o = ops[k.op];
-                if (o.kind == BI_OP_QUANTIZE_ACT) continue;
+                if (o.kind != BI_OP_LINEAR && o.kind != BI_OP_LMHEAD) continue;
                 k.u = range_start(blockIdx.x, o.units, G);
                 k.ue = range_start(blockIdx.x + 1, o.units, G);
                 if (k.u < k.ue) {
@@ -340,38 +341,41 @@ __global__ void __launch_bounds__(kThreads, 2) program_kernel(const ProgHeader *
             consumer_bar();
         }
 
-        if (op.kind == BI_OP_QUANTIZE_ACT) {
-            // --------------------------------------------------- quantise rows
-            // rows (m + row_shift) % G == this CTA; 256 threads per row
+        if (op.kind != BI_OP_LINEAR && op.kind != BI_OP_LMHEAD) {
+            // ------------------------------------------ quantise rows (three kinds)
+            // rows (m + row_shift) % G == this CTA; 256 threads per row.  The
+            // row's input: x (plain), bf16(h + x) rescaled (residual, h = op.y
+            // updated in place), or bf16(relu(x[:, :K]) * x[:, K:2K]).
+            const int kind = op.kind;
             int rows_here = 0;
             for (int m = (static_cast<int>(blockIdx.x) - op.row_shift % G + G) % G; m < op.M; m += G) {
                 ++rows_here;
                 constexpr int kT = kConsumerWarps * 32;
                 constexpr int kRegChunks = 8;   // rows up to 8 * kT * 8 = 16384 values stay in registers
                 const uint16_t *xr = op.x + static_cast<long long>(m) * op.ldx;
+                uint16_t *hr = op.y ? op.y + static_cast<long long>(m) * op.K : nullptr;
                 const int nchunk = op.K / 8;
                 const bool in_regs = nchunk <= kRegChunks * kT;
+                auto load_in = [&](int ci) -> uint4 {
+                    const uint4 a = *reinterpret_cast<const uint4 *>(xr + ci * 8);
+                    if (kind == BI_OP_RESIDUAL_QUANT)
+                        return residual8(*reinterpret_cast<const uint4 *>(hr + ci * 8), a);
+                    if (kind == BI_OP_RELU_MUL_QUANT)
+                        return relu_mul8(a, *reinterpret_cast<const uint4 *>(xr + op.K + ci * 8));
+                    return a;
+                };
                 float amax = 0.0f;
                 uint4 v[kRegChunks];
 #pragma unroll
                 for (int c = 0; c < kRegChunks; ++c) {
                     const int ci = c * kT + ctid;
-                    v[c] = (in_regs && ci < nchunk) ? *reinterpret_cast<const uint4 *>(xr + ci * 8)
-                                                    : make_uint4(0, 0, 0, 0);
+                    v[c] = (in_regs && ci < nchunk) ? load_in(ci) : make_uint4(0, 0, 0, 0);
                 }
-                auto absmax8 = [&](const uint4 &t) {
-                    const uint32_t w4[4] = {t.x, t.y, t.z, t.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        amax = fmaxf(amax, fabsf(__uint_as_float(w4[e] << 16)));
-                        amax = fmaxf(amax, fabsf(__uint_as_float(w4[e] & 0xFFFF0000u)));
-                    }
-                };
                 if (in_regs) {
 #pragma unroll
-                    for (int c = 0; c < kRegChunks; ++c) absmax8(v[c]);
+                    for (int c = 0; c < kRegChunks; ++c) amax = absmax8(v[c], amax);
                 } else {
-                    for (int ci = ctid; ci < nchunk; ci += kT) absmax8(*reinterpret_cast<const uint4 *>(xr + ci * 8));
+                    for (int ci = ctid; ci < nchunk; ci += kT) amax = absmax8(load_in(ci), amax);
                 }
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
@@ -381,15 +385,27 @@ __global__ void __launch_bounds__(kThreads, 2) program_kernel(const ProgHeader *
 #pragma unroll
                 for (int w = 0; w < kConsumerWarps; ++w) amax = fmaxf(amax, sq[w]);
                 consumer_bar();
+                int p2 = 0;
+                if (kind == BI_OP_RESIDUAL_QUANT) {
+                    p2 = rescale_shift(amax);
+                    amax = scale_pow2(amax, p2);   // exact: the rescaled row's largest magnitude
+                }
                 const float s = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 127.0f);
                 const float r = __frcp_rn(s);
-                auto quant8 = [&](const uint4 &t, int ci) {
+                // each thread writes only chunks it read itself (in-place h is safe)
+                auto emit = [&](uint4 t, int ci) {
+                    if (kind == BI_OP_RESIDUAL_QUANT) {
+                        t = rescale8(t, p2);
+                        *reinterpret_cast<uint4 *>(hr + ci * 8) = t;
+                    } else if (kind == BI_OP_RELU_MUL_QUANT && hr) {
+                        *reinterpret_cast<uint4 *>(hr + ci * 8) = t;
+                    }
                     const uint32_t w4[4] = {t.x, t.y, t.z, t.w};
                     uint32_t o[2] = {0, 0};
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const int lo = quant_code(__uint_as_float(w4[e] << 16), s, r);
-                        const int hi = quant_code(__uint_as_float(w4[e] & 0xFFFF0000u), s, r);
+                        const int lo = quant_code(bf16_lo(w4[e]), s, r);
+                        const int hi = quant_code(bf16_hi(w4[e]), s, r);
                         o[e >> 1] |= ((static_cast<uint32_t>(lo) & 0xFFu) | ((static_cast<uint32_t>(hi) & 0xFFu) << 8))
                                      << (16 * (e & 1));
                     }
@@ -399,10 +415,10 @@ __global__ void __launch_bounds__(kThreads, 2) program_kernel(const ProgHeader *
 #pragma unroll
                     for (int c = 0; c < kRegChunks; ++c) {
                         const int ci = c * kT + ctid;
-                        if (ci < nchunk) quant8(v[c], ci);
+                        if (ci < nchunk) emit(v[c], ci);
                     }
                 } else {
-                    for (int ci = ctid; ci < nchunk; ci += kT) quant8(*reinterpret_cast<const uint4 *>(xr + ci * 8), ci);
+                    for (int ci = ctid; ci < nchunk; ci += kT) emit(load_in(ci), ci);
                 }
                 if (ctid == 0) op.s_a[m] = s;
                 fence_proxy_async_global();   // the codes are read by other CTAs' TMA
@@ -690,6 +706,39 @@ bool encode(CUtensorMap *map, const void *base, long long rows, long long cols, 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool is_quantising(int kind)
+{
+    return kind == BI_OP_QUANTIZE_ACT || kind == BI_OP_RESIDUAL_QUANT || kind == BI_OP_RELU_MUL_QUANT;
+}
+
+bool is_matmul(int kind) { return kind == BI_OP_LINEAR || kind == BI_OP_LMHEAD; }
+
+// A byte range of device memory.
+struct Range {
+    const void *p;
+    size_t n;
+    bool meets(const Range &o) const
+    {
+        if (!p || !o.p || !n || !o.n) return false;
+        const char *a = static_cast<const char *>(p), *b = static_cast<const char *>(o.p);
+        return a < b + o.n && b < a + n;
+    }
+};
+
+// What a quantising op reads: x (K or 2K columns per row) and, for the
+// residual kind, the stream h it also writes.  Returns the number of ranges.
+int quant_inputs(const bi_op &o, Range (&in)[2])
+{
+    if (!is_quantising(o.kind)) return 0;
+    const size_t width = (o.kind == BI_OP_RELU_MUL_QUANT) ? 2 * static_cast<size_t>(o.K) : o.K;
+    in[0] = {o.x, (static_cast<size_t>(o.M > 0 ? o.M : 1) - 1) * o.ldx * 2 + width * 2};
+    if (o.kind == BI_OP_RESIDUAL_QUANT) {
+        in[1] = {o.y, static_cast<size_t>(o.M) * o.K * 2};
+        return 2;
+    }
+    return 1;
+}
+
 bool a16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool a4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
@@ -738,18 +787,16 @@ BI_API bi_status bi_program_build(const bi_op *ops, int n_ops, void *program, si
         d.qwait = 0;
         if (i > 0) {
             const bi_op &p = ops[i - 1];
-            const bool reads_prev_quant = (o.kind == BI_OP_LINEAR || o.kind == BI_OP_LMHEAD) &&
-                                          p.kind == BI_OP_QUANTIZE_ACT && p.q == o.q && p.s_a == o.s_a &&
-                                          p.M == o.M && p.K == o.K;
-            // the op's outputs must not be the quantisation's input (a write
+            const bool reads_prev_quant = is_matmul(o.kind) && is_quantising(p.kind) && p.q == o.q &&
+                                          p.s_a == o.s_a && p.M == o.M && p.K == o.K;
+            // the op's outputs must not be what the quantisation read (a write
             // could race with its reads)
-            const char *x0 = reinterpret_cast<const char *>(p.x);
-            const char *x1 = x0 + (static_cast<size_t>(p.M) - 1) * p.ldx * 2 + static_cast<size_t>(p.K) * 2;
-            const char *y0 = reinterpret_cast<const char *>(o.y);
-            const char *y1 = y0 ? y0 + static_cast<size_t>(o.M) * o.N * 2 : y0;
-            const char *a0 = reinterpret_cast<const char *>(o.argmax);
-            const char *a1 = a0 ? a0 + static_cast<size_t>(o.M) * 4 : a0;
-            const bool overlap = (y0 && y0 < x1 && x0 < y1) || (a0 && a0 < x1 && x0 < a1);
+            Range in[2];
+            const int n_in = quant_inputs(p, in);
+            const Range y = {o.y, o.y ? static_cast<size_t>(o.M) * o.N * 2 : 0};
+            const Range am = {o.argmax, o.argmax ? static_cast<size_t>(o.M) * 4 : 0};
+            bool overlap = false;
+            for (int t = 0; t < n_in; ++t) overlap = overlap || in[t].meets(y) || in[t].meets(am);
             if (reads_prev_quant && !overlap) {
                 d.qwait = rows_quantised;
             } else {
@@ -758,13 +805,23 @@ BI_API bi_status bi_program_build(const bi_op *ops, int n_ops, void *program, si
         }
         if (o.M < 1 || o.K < 16 || (o.K % 16) != 0) return BI_ERR_INVALID_ARG;
         if (o.K > 133144) return BI_ERR_INT32_BOUND;
-        if (o.kind == BI_OP_QUANTIZE_ACT) {
-            if (!o.x || !o.q || !o.s_a || o.ldx < o.K || o.M > 65535) return BI_ERR_INVALID_ARG;
-            if (!a16(o.x) || !a16(o.q) || !a4(o.s_a) || (o.ldx % 8) != 0) return BI_ERR_ALIGNMENT;
+        if (is_quantising(o.kind)) {
+            const long long width = (o.kind == BI_OP_RELU_MUL_QUANT) ? 2LL * o.K : o.K;
+            if (!o.x || !o.q || !o.s_a || o.ldx < width || o.M > 65535) return BI_ERR_INVALID_ARG;
+            if (o.kind == BI_OP_RESIDUAL_QUANT && !o.y) return BI_ERR_INVALID_ARG;
+            if (!a16(o.x) || !a16(o.q) || !a4(o.s_a) || (o.ldx % 8) != 0 || (o.y && !a16(o.y)))
+                return BI_ERR_ALIGNMENT;
+            if (o.kind == BI_OP_QUANTIZE_ACT && o.y) return BI_ERR_INVALID_ARG;
+            // h (or m) is written while x is read: they may not share memory
+            Range in[2];
+            quant_inputs(o, in);
+            const Range out = {o.y, o.y ? static_cast<size_t>(o.M) * o.K * 2 : 0};
+            if (out.meets(in[0])) return BI_ERR_INVALID_ARG;
             d.x = o.x;
             d.ldx = o.ldx;
             d.q = o.q;
             d.s_a = o.s_a;
+            d.y = o.y;
             d.row_shift = (i * 37) & 1023;
             rows_quantised += o.M;
         } else if (o.kind == BI_OP_LINEAR || o.kind == BI_OP_LMHEAD) {

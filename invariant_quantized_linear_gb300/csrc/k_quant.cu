@@ -9,12 +9,15 @@
 // requantising the codes, not by rewriting the scales.
 #include "kernels.cuh"
 #include "ptx.cuh"
+#include "row_ops.cuh"
 
 namespace bi {
 
 namespace {
 
 constexpr int kQuantThreads = 256;
+
+enum RowMode { kRowPlain = 0, kRowResidual = 1, kRowReluMul = 2 };
 
 template <int THREADS = kQuantThreads>
 __device__ __forceinline__ float block_max(float v, float *red)
@@ -111,17 +114,44 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_rows_kernel(const void
     if (threadIdx.x == 0) s_out[row] = s;
 }
 
-// Activation rows up to 16384 elements: one CTA of 256 threads per row, each
-// thread holding C chunks of 8 bf16 values in registers, so the row is read
-// from memory once and the kernel is one load, one block reduction and one
-// store deep.  The CTA is small so that it fits beside a running linear-layer
-// CTA when launched as a programmatic dependent.
+// Activation rows: one CTA of 256 threads per row.  For rows up to 16384
+// elements each thread holds C chunks of 8 bf16 values in registers, so the
+// row is read from memory once and the kernel is one load, one block
+// reduction and one store deep; longer rows (C = 0) are read twice.  The CTA
+// is small so that it fits beside a running linear-layer CTA when launched as
+// a programmatic dependent.
+//
+// MODE selects the row's input (the elementwise steps of row_ops.cuh):
+//   kRowPlain     x[row]
+//   kRowResidual  bf16_rne(h[row] + x[row]), rescaled by 2^-ilogb(absmax) and
+//                 written back to h (in place, row stride K)
+//   kRowReluMul   bf16_rne(relu(x[row, :K]) * x[row, K:2K]), written to h if
+//                 h is not null
+// and the quantised codes are those of that input.
 constexpr int kActThreads = 256;
 
-template <int C>
-__global__ void __launch_bounds__(kActThreads) quantize_act_reg_kernel(const uint16_t *__restrict__ x, int64_t ldx,
-                                                                       int K, int8_t *__restrict__ q,
-                                                                       float *__restrict__ s_out, int pdl)
+struct RowArgs {
+    const uint16_t *x;
+    int64_t ldx;
+    uint16_t *h;
+    int K;
+    int8_t *q;
+    float *s_a;
+};
+
+__device__ __forceinline__ uint4 ld16(const uint16_t *p) { return *reinterpret_cast<const uint4 *>(p); }
+
+template <int MODE>
+__device__ __forceinline__ uint4 row_in8(const RowArgs &a, int64_t row, int k)
+{
+    const uint16_t *xr = a.x + row * a.ldx;
+    if constexpr (MODE == kRowResidual) return residual8(ld16(a.h + row * a.K + k), ld16(xr + k));
+    if constexpr (MODE == kRowReluMul) return relu_mul8(ld16(xr + k), ld16(xr + a.K + k));
+    return ld16(xr + k);
+}
+
+template <int C, int MODE>
+__global__ void __launch_bounds__(kActThreads) row_quant_kernel(RowArgs a, int pdl)
 {
     __shared__ float red[kActThreads / 32];
     if (pdl) {
@@ -129,38 +159,84 @@ __global__ void __launch_bounds__(kActThreads) quantize_act_reg_kernel(const uin
         pdl_wait();
     }
     const int64_t row = blockIdx.x;
-    const uint16_t *xr = x + row * ldx;
-    uint4 v[C];
+    const int K = a.K;
+    uint4 v[C > 0 ? C : 1];
     float amax = 0.0f;
+    if constexpr (C > 0) {
 #pragma unroll
-    for (int c = 0; c < C; ++c) {
-        const int k = (c * kActThreads + threadIdx.x) * 8;
-        v[c] = (k < K) ? *reinterpret_cast<const uint4 *>(xr + k) : make_uint4(0, 0, 0, 0);
-        const uint32_t w[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            amax = fmaxf(amax, fabsf(__uint_as_float(w[i] << 16)));
-            amax = fmaxf(amax, fabsf(__uint_as_float(w[i] & 0xFFFF0000u)));
+        for (int c = 0; c < C; ++c) {
+            const int k = (c * kActThreads + threadIdx.x) * 8;
+            v[c] = (k < K) ? row_in8<MODE>(a, row, k) : make_uint4(0, 0, 0, 0);
+            amax = absmax8(v[c], amax);
         }
+    } else {
+        for (int k = threadIdx.x * 8; k < K; k += kActThreads * 8) amax = absmax8(row_in8<MODE>(a, row, k), amax);
     }
     amax = block_max<kActThreads>(amax, red);
+    int p = 0;
+    if constexpr (MODE == kRowResidual) {
+        p = rescale_shift(amax);
+        amax = scale_pow2(amax, p);   // exact: the row's largest magnitude, rescaled
+    }
     const float s = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 127.0f);
-    int8_t *qr = q + row * K;
-#pragma unroll
-    for (int c = 0; c < C; ++c) {
-        const int k = (c * kActThreads + threadIdx.x) * 8;
-        if (k >= K) continue;
-        const uint32_t w[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
+    int8_t *qr = a.q + row * K;
+    // Each thread writes only the chunks it read itself, so the in-place
+    // residual update never overwrites a value another thread has yet to read.
+    auto emit = [&](uint4 t, int k) {
+        if constexpr (MODE == kRowResidual) {
+            t = rescale8(t, p);
+            *reinterpret_cast<uint4 *>(a.h + row * K + k) = t;
+        }
+        if constexpr (MODE == kRowReluMul) {
+            if (a.h) *reinterpret_cast<uint4 *>(a.h + row * K + k) = t;
+        }
+        const uint32_t w[4] = {t.x, t.y, t.z, t.w};
         uint32_t o[2] = {0, 0};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const uint32_t lo = static_cast<uint8_t>(quant1(__uint_as_float(w[i] << 16), s));
-            const uint32_t hi = static_cast<uint8_t>(quant1(__uint_as_float(w[i] & 0xFFFF0000u), s));
+            const uint32_t lo = static_cast<uint8_t>(quant1(bf16_lo(w[i]), s));
+            const uint32_t hi = static_cast<uint8_t>(quant1(bf16_hi(w[i]), s));
             o[i >> 1] |= (lo | (hi << 8)) << (16 * (i & 1));
         }
         *reinterpret_cast<uint2 *>(qr + k) = make_uint2(o[0], o[1]);
+    };
+    if constexpr (C > 0) {
+#pragma unroll
+        for (int c = 0; c < C; ++c) {
+            const int k = (c * kActThreads + threadIdx.x) * 8;
+            if (k < K) emit(v[c], k);
+        }
+    } else {
+        for (int k = threadIdx.x * 8; k < K; k += kActThreads * 8) emit(row_in8<MODE>(a, row, k), k);
     }
-    if (threadIdx.x == 0) s_out[row] = s;
+    if (threadIdx.x == 0) a.s_a[row] = s;
+}
+
+template <int MODE>
+cudaError_t launch_rows(const RowArgs &a, int M, bool pdl, cudaStream_t stream)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(M));
+    cfg.blockDim = dim3(kActThreads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    const int p = pdl ? 1 : 0;
+    const int chunks = (a.K + kActThreads * 8 - 1) / (kActThreads * 8);
+    switch (chunks) {
+    case 1: return cudaLaunchKernelEx(&cfg, row_quant_kernel<1, MODE>, a, p);
+    case 2: return cudaLaunchKernelEx(&cfg, row_quant_kernel<2, MODE>, a, p);
+    case 3: return cudaLaunchKernelEx(&cfg, row_quant_kernel<3, MODE>, a, p);
+    case 4: return cudaLaunchKernelEx(&cfg, row_quant_kernel<4, MODE>, a, p);
+    case 5: return cudaLaunchKernelEx(&cfg, row_quant_kernel<5, MODE>, a, p);
+    case 6: return cudaLaunchKernelEx(&cfg, row_quant_kernel<6, MODE>, a, p);
+    case 7: return cudaLaunchKernelEx(&cfg, row_quant_kernel<7, MODE>, a, p);
+    case 8: return cudaLaunchKernelEx(&cfg, row_quant_kernel<8, MODE>, a, p);
+    default: return cudaLaunchKernelEx(&cfg, row_quant_kernel<0, MODE>, a, p);
+    }
 }
 
 // Round the integer p / 2^sh to nearest, ties to even (sh >= 1), symmetric in sign.
@@ -242,30 +318,22 @@ __global__ void __launch_bounds__(kQuantThreads) requant_pow2_kernel(const int8_
 cudaError_t launch_quantize_act(const uint16_t *x, int64_t ldx, int M, int K, int8_t *q, float *s_a, bool pdl,
                                 cudaStream_t stream)
 {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(M));
-    cfg.blockDim = dim3(kActThreads);
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = pdl ? 1 : 0;
-    const int p = pdl ? 1 : 0;
-    const int chunks = (K + kActThreads * 8 - 1) / (kActThreads * 8);
-    switch (chunks) {
-    case 1: return cudaLaunchKernelEx(&cfg, quantize_act_reg_kernel<1>, x, ldx, K, q, s_a, p);
-    case 2: return cudaLaunchKernelEx(&cfg, quantize_act_reg_kernel<2>, x, ldx, K, q, s_a, p);
-    case 3: return cudaLaunchKernelEx(&cfg, quantize_act_reg_kernel<3>, x, ldx, K, q, s_a, p);
-    case 4: return cudaLaunchKernelEx(&cfg, quantize_act_reg_kernel<4>, x, ldx, K, q, s_a, p);
-    case 5: return cudaLaunchKernelEx(&cfg, quantize_act_reg_kernel<5>, x, ldx, K, q, s_a, p);
-    case 6: return cudaLaunchKernelEx(&cfg, quantize_act_reg_kernel<6>, x, ldx, K, q, s_a, p);
-    case 7: return cudaLaunchKernelEx(&cfg, quantize_act_reg_kernel<7>, x, ldx, K, q, s_a, p);
-    case 8: return cudaLaunchKernelEx(&cfg, quantize_act_reg_kernel<8>, x, ldx, K, q, s_a, p);
-    default: break;
-    }
-    cfg.blockDim = dim3(kQuantThreads);
-    return cudaLaunchKernelEx(&cfg, quantize_rows_kernel<true>, static_cast<const void *>(x), ldx, K, q, s_a, p);
+    const RowArgs a = {x, ldx, nullptr, K, q, s_a};
+    return launch_rows<kRowPlain>(a, M, pdl, stream);
+}
+
+cudaError_t launch_residual_quantize(uint16_t *h, const uint16_t *y, int64_t ldy, int M, int K, int8_t *q,
+                                     float *s_a, bool pdl, cudaStream_t stream)
+{
+    const RowArgs a = {y, ldy, h, K, q, s_a};
+    return launch_rows<kRowResidual>(a, M, pdl, stream);
+}
+
+cudaError_t launch_relu_mul_quantize(const uint16_t *gu, int64_t ldgu, int M, int K, int8_t *q, float *s_a,
+                                     uint16_t *m_out, bool pdl, cudaStream_t stream)
+{
+    const RowArgs a = {gu, ldgu, m_out, K, q, s_a};
+    return launch_rows<kRowReluMul>(a, M, pdl, stream);
 }
 
 cudaError_t launch_quantize_weight(const float *w, int64_t ldw, int N, int K, int8_t *w_q, float *s_w,

@@ -157,38 +157,41 @@ def relu_mul(gu: np.ndarray, K: int) -> np.ndarray:
     return out
 
 
-def verify_pass(h0: np.ndarray, layers, head, q_rows: int, record: bool = False):
-    """Chained verify pass over a stack of W8A8 layers, then the greedy head.
-
-    h0: uint16 [M, H] bf16 residual stream entering layer 0.
-    layers: sequence of dicts with int8 codes and fp32 scales
-        "qkv": (wq [q_rows + 2*kv, H], s_w)  q, k, v rows packed in that order
+def chain_layer(h: np.ndarray, L, q_rows: int):
+    """One layer of the chained verify pass on the residual stream h (uint16
+    [M, H] bf16).  L: dict of int8 codes and fp32 scales
+        "qkv": (wq [q_rows + 2*kv, H], s_w)  q, k, v rows packed in that order,
         "o": (wq [H, q_rows], s_w), "gu": (wq [2*I, H], s_w)  gate rows then up rows,
         "down": (wq [H, I], s_w).
-    head: (wq [V, H], s_w).
-    Per layer:  q_h = quant(h);  y_qkv = lin(q_h, qkv);  a = y_qkv[:, :q_rows]
-    (attention stand-in; k and v are computed and returned, not used);
-    h = residual_rescale(h, lin(quant(a), o));  y_gu = lin(quant(h), gu);
-    h = residual_rescale(h, lin(quant(relu_mul(y_gu)), down)).
-    Then argmax = head(quant(h)).  Returns (argmax int32 [M], h, records) with
-    records, if asked, the per-layer dict of every linear output and h."""
+    Steps:  y_qkv = lin(quant(h), qkv);  a = y_qkv[:, :q_rows] (attention
+    stand-in; k and v are computed, not used);  h = residual_rescale(h,
+    lin(quant(a), o));  y_gu = lin(quant(h), gu);  h = residual_rescale(h,
+    lin(quant(relu_mul(y_gu)), down)).  Returns (new h, dict of every linear
+    output and of h after the first residual)."""
+    q, s = quantize_act(h)
+    y_qkv = linear_w8a8(q, s, *L["qkv"])
+    qa, sa = quantize_act(np.ascontiguousarray(y_qkv[:, :q_rows]))
+    y_o = linear_w8a8(qa, sa, *L["o"])
+    h_mid = residual_rescale(h, y_o)
+    q, s = quantize_act(h_mid)
+    y_gu = linear_w8a8(q, s, *L["gu"])
+    inter = L["gu"][0].shape[0] // 2
+    mq, ms = quantize_act(relu_mul(y_gu, inter))
+    y_d = linear_w8a8(mq, ms, *L["down"])
+    h_new = residual_rescale(h_mid, y_d)
+    return h_new, {"qkv": y_qkv, "o": y_o, "h_mid": h_mid, "gu": y_gu, "down": y_d, "h": h_new}
+
+
+def verify_pass(h0: np.ndarray, layers, head, q_rows: int, record: bool = False):
+    """Chained verify pass: chain_layer over `layers` from h0, then the greedy
+    head (wq [V, H], s_w) on quant(h).  Returns (argmax int32 [M], final h,
+    per-layer records of chain_layer if asked, else [])."""
     h = np.array(_c(h0, np.uint16), copy=True)
     recs = []
     for L in layers:
-        q, s = quantize_act(h)
-        y_qkv = linear_w8a8(q, s, *L["qkv"])
-        qa, sa = quantize_act(np.ascontiguousarray(y_qkv[:, :q_rows]))
-        y_o = linear_w8a8(qa, sa, *L["o"])
-        h = residual_rescale(h, y_o)
-        h_mid = h
-        q, s = quantize_act(h)
-        y_gu = linear_w8a8(q, s, *L["gu"])
-        inter = L["gu"][0].shape[0] // 2
-        mq, ms = quantize_act(relu_mul(y_gu, inter))
-        y_d = linear_w8a8(mq, ms, *L["down"])
-        h = residual_rescale(h, y_d)
+        h, rec = chain_layer(h, L, q_rows)
         if record:
-            recs.append({"qkv": y_qkv, "o": y_o, "h_mid": h_mid, "gu": y_gu, "down": y_d, "h": h})
+            recs.append(rec)
     q, s = quantize_act(h)
     am, _ = lmhead_argmax(q, s, *head, want_logits=False)
     return am, h, recs

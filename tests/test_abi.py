@@ -108,3 +108,39 @@ def test_workspace_status_validation(bi):
 def test_valid_call_without_gpu_is_unsupported(bi):
     wsb = bi.bi_linear_workspace_size(2, 1024, 1024)
     assert _lin(bi, wsb=wsb) == bi.BI_ERR_UNSUPPORTED
+
+
+def test_fused_quantize_validation(bi):
+    R = bi.lib.bi_residual_quantize
+    F2 = FAKE + (1 << 20)
+    assert R(None, F2, 1024, 2, 1024, FAKE, FAKE, 0, None) == bi.BI_ERR_INVALID_ARG
+    assert R(FAKE, F2, 512, 2, 1024, FAKE, FAKE, 0, None) == bi.BI_ERR_INVALID_ARG       # ldy < K
+    assert R(FAKE, F2, 1024, 2, 1000, FAKE, FAKE, 0, None) == bi.BI_ERR_INVALID_ARG      # K % 16
+    assert R(FAKE, F2 + 8, 1024, 2, 1024, FAKE, FAKE, 0, None) == bi.BI_ERR_ALIGNMENT
+    assert R(FAKE, F2, 1028, 2, 1024, FAKE, FAKE, 0, None) == bi.BI_ERR_ALIGNMENT        # ldy % 8
+    assert R(FAKE, FAKE + 2048, 1024, 2, 1024, F2, F2 + 4096, 0, None) == bi.BI_ERR_INVALID_ARG  # y inside h
+    assert R(FAKE, F2, 1024, 2, 1024, FAKE + 1024, F2 + 8192, 0, None) == bi.BI_ERR_INVALID_ARG  # q inside h
+    G = bi.lib.bi_relu_mul_quantize
+    assert G(FAKE, 1024, 2, 1024, F2, F2 + 4096, None, 0, None) == bi.BI_ERR_INVALID_ARG   # ldgu < 2K
+    assert G(FAKE, 2048, 2, 1024, F2 + 4, F2 + 4096, None, 0, None) == bi.BI_ERR_ALIGNMENT
+    assert G(FAKE, 2048, 2, 1024, F2, F2 + 4096, FAKE + 4096, 0, None) == bi.BI_ERR_INVALID_ARG  # m_out in gu
+
+
+def test_program_build_validation(bi):
+    F2 = FAKE + (1 << 20)
+    prog_bytes = bi.bi_program_bytes(1)
+    prog = F2 + (1 << 20)          # never written: validation fails first
+    def one(**kw):
+        f = dict(kind=bi.BI_OP_RESIDUAL_QUANT, M=2, N=0, K=1024, x=FAKE, ldx=1024, q=F2, s_a=F2 + 4096,
+                 w_q=None, s_w=None, y=FAKE + 8192, argmax=None)
+        f.update(kw)
+        op = bi.bi_op(*[f[k] for k in ("kind", "M", "N", "K", "x", "ldx", "q", "s_a", "w_q", "s_w", "y",
+                                       "argmax")])
+        return bi.lib.bi_program_build(ctypes.byref(op), 1, prog, prog_bytes)
+    assert one(y=None) == bi.BI_ERR_INVALID_ARG                                # residual needs h
+    assert one(y=FAKE + 1024) == bi.BI_ERR_INVALID_ARG                         # h overlaps x
+    assert one(ldx=1028) == bi.BI_ERR_ALIGNMENT
+    assert one(kind=bi.BI_OP_RELU_MUL_QUANT, ldx=1024, y=None) == bi.BI_ERR_INVALID_ARG   # ldx < 2K
+    assert one(kind=bi.BI_OP_RELU_MUL_QUANT, ldx=2048, y=FAKE + 2048) == bi.BI_ERR_INVALID_ARG  # m in gu
+    assert one(kind=bi.BI_OP_QUANTIZE_ACT, y=FAKE + 8192) == bi.BI_ERR_INVALID_ARG  # plain kind has no y
+    assert one(kind=9) == bi.BI_ERR_INVALID_ARG
