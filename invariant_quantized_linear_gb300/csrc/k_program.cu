@@ -36,6 +36,7 @@ namespace {
 
 using namespace stream;
 using Gp = Geo<2>;   // eight consumer warps per CTA, two CTAs per SM (measured best)
+
 constexpr int kKSplit = Gp::kKSplit;
 constexpr int kConsumerWarps = Gp::kConsumerWarps;
 constexpr int kThreads = Gp::kThreads;
@@ -78,10 +79,12 @@ struct PCfg {
     static constexpr int kAStage = kNch * kAChunkBytes;                 // 2 or 4 KB
     static constexpr int kStages = (MT == 1) ? 5 : 4;                   // two CTAs per SM
     static constexpr int kRedBytes = (kKSplit - 1) * kBM * kMaxTok * 4;
+    // a deferred run's slot values after its adds: [4 row groups x 32 lanes][MT * 4] uint64
+    static constexpr int kDeferBytes = 4 * 32 * MT * 4 * 8;
     // full, empty, pend_map (8 B each per stage), sbest, pend_bar/qw/c (4 B each per stage), flags, sq
     static constexpr int kCtlBytes =
         3 * kStages * 8 + kConsumerWarps * kMaxTok * 8 + 3 * kStages * 4 + 16 * 4 + kConsumerWarps * 4;
-    static constexpr int kSmemBytes = kStages * (kWStage + kAStage) + kRedBytes + 1024 + kCtlBytes;
+    static constexpr int kSmemBytes = kStages * (kWStage + kAStage) + kRedBytes + kDeferBytes + 1024 + kCtlBytes;
 };
 
 __device__ __forceinline__ int ld_acquire_gpu(const int *p)
@@ -110,13 +113,15 @@ __device__ __forceinline__ void consumer_bar()
 
 // Workspace of a program run (its own layout: up to kProgMaxGrid CTAs):
 //   [0, 256)  status, argmax ticket, barrier arrivals, exit ticket, rows quantised
-//   rb_counter [kProgMaxGrid] int32, best [kProgMaxGrid][16] uint64,
-//   partial [kProgMaxGrid][64][16] int32
+//   best [kProgMaxGrid][16] uint64, partial [kProgMaxGrid][64][16] uint64
+// A partial slot holds, per element of a row block shared by several CTAs,
+// (K units summed so far) * 2^40 + (their int32 partial sum), as one 64-bit
+// integer, so one atomic add both accumulates a contribution and tells its
+// issuer whether it completed the element.
 constexpr int kProgMaxGrid = 512;
-constexpr size_t kPwCounterOff = 256;
-constexpr size_t kPwBestOff = kPwCounterOff + sizeof(int32_t) * kProgMaxGrid;
+constexpr size_t kPwBestOff = 256;
 constexpr size_t kPwPartialOff = kPwBestOff + sizeof(unsigned long long) * kProgMaxGrid * kMaxTok;
-constexpr size_t kPwBytes = kPwPartialOff + sizeof(int32_t) * kProgMaxGrid * kBM * kMaxTok;
+constexpr size_t kPwBytes = kPwPartialOff + sizeof(unsigned long long) * kProgMaxGrid * kBM * kMaxTok;
 
 struct ProgWs {
     int *status;
@@ -124,9 +129,8 @@ struct ProgWs {
     int *bar;            // grid barrier arrivals (G per barrier)
     int *exit_ticket;
     int *qdone;          // activation rows quantised so far in this run
-    int32_t *rb_counter;
     unsigned long long *best;
-    int32_t *partial;
+    unsigned long long *partial;
 };
 
 template <int MT>
@@ -138,9 +142,11 @@ __global__ void __launch_bounds__(kThreads, 2) program_kernel(const ProgHeader *
     uint8_t *sW = smem;
     uint8_t *sA = smem + C::kStages * C::kWStage;
     int32_t *sred = reinterpret_cast<int32_t *>(sA + C::kStages * C::kAStage);
+    unsigned long long *sdefer = reinterpret_cast<unsigned long long *>(sA + C::kStages * C::kAStage + C::kRedBytes);
     // control area: 8-byte fields first, then 4-byte ones, so every field is
     // naturally aligned whatever the stage count
-    uint64_t *full = reinterpret_cast<uint64_t *>(sA + C::kStages * C::kAStage + C::kRedBytes);
+    uint64_t *full =
+        reinterpret_cast<uint64_t *>(sA + C::kStages * C::kAStage + C::kRedBytes + C::kDeferBytes);
     uint64_t *empty = full + C::kStages;
     // per ring stage, for a use whose activation tile is not yet requested:
     const CUtensorMap **pend_map = reinterpret_cast<const CUtensorMap **>(empty + C::kStages);  // its q descriptor
@@ -148,9 +154,8 @@ __global__ void __launch_bounds__(kThreads, 2) program_kernel(const ProgHeader *
     int *pend_bar = reinterpret_cast<int *>(sbest + kConsumerWarps * kMaxTok);               // barrier to pass
     int *pend_qw = pend_bar + C::kStages;                                                    // or rows to await
     int *pend_c = pend_qw + C::kStages;                                                      // its K unit
-    volatile int *flags = reinterpret_cast<volatile int *>(pend_c + C::kStages);  // abort, last[2]
+    volatile int *flags = reinterpret_cast<volatile int *>(pend_c + C::kStages);  // abort
     volatile int *abort_flag = flags;
-    volatile int *last_flag = flags + 1;
     float *sq = reinterpret_cast<float *>(const_cast<int *>(flags) + 16);        // [kConsumerWarps] quant reduce
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -167,7 +172,6 @@ __global__ void __launch_bounds__(kThreads, 2) program_kernel(const ProgHeader *
             mbar_init(&empty[s], kConsumerWarps);
         }
         *abort_flag = 0;
-        last_flag[0] = last_flag[1] = 0;
         fence_mbarrier_init();
     }
     __syncthreads();
@@ -211,8 +215,17 @@ __global__ void __launch_bounds__(kThreads, 2) program_kernel(const ProgHeader *
                 }
             }
         };
+        auto advance = [&](Cursor &k) {
+            if (++k.u == k.ue) {
+                seek(k, k.op + 1);
+            } else if (++k.c == k.upr) {
+                k.c = 0;
+                ++k.rb;
+            }
+        };
         Cursor wc;           // next unit to load into the ring
         seek(wc, 0);
+
         // request activation tiles of every use whose op's barrier has passed
         int seen_q = 0;      // last value read from the rows-quantised counter
         auto issue_ready_a = [&](bool refresh) {
@@ -266,12 +279,7 @@ __global__ void __launch_bounds__(kThreads, 2) program_kernel(const ProgHeader *
             pend_qw[s] = wc.qwait;
             pend_c[s] = wc.c;
             ++j;
-            if (++wc.u == wc.ue) {
-                seek(wc, wc.op + 1);
-            } else if (++wc.c == wc.upr) {
-                wc.c = 0;
-                ++wc.rb;
-            }
+            advance(wc);
             issue_ready_a(false);
             t0 = global_timer_ns();
         }
@@ -451,31 +459,61 @@ __global__ void __launch_bounds__(kThreads, 2) program_kernel(const ProgHeader *
             sw[0] = n0 < op.N ? op.s_w[n0] : 0.0f;
             sw[1] = n0 + 8 < op.N ? op.s_w[n0 + 8] : 0.0f;
         };
-        auto epilogue = [&](int rb, const int32_t (&v)[MT][4], const float (&sw)[2]) {
-            const int n0 = rb * kBM + rg * 16 + g;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int n = n0 + ((e & 2) ? 8 : 0);
-                if (n >= op.N) continue;
-#pragma unroll
-                for (int t = 0; t < MT; ++t) {
-                    const int tok = 8 * t + 2 * tq + (e & 1);
-                    if (tok >= op.M) continue;
-                    float f = __int2float_rn(v[t][e]);
-                    f = __fmul_rn(f, sa_reg[t][e & 1]);
-                    f = __fmul_rn(f, sw[(e & 2) ? 1 : 0]);
-                    const uint16_t b = __bfloat16_as_ushort(__float2bfloat16_rn(f));
-                    if (op.y) op.y[static_cast<size_t>(tok) * op.N + n] = b;
-                    if (head) {
-                        const unsigned long long key = argmax_key(b, n);
-                        if (key > best[t][e & 1]) best[t][e & 1] = key;
-                    }
-                }
+        // y[tok, n] (and the argmax key) of one accumulator element
+        auto emit1 = [&](int rb, int t, int e, int32_t acc, const float (&sw)[2]) {
+            const int n = rb * kBM + rg * 16 + g + ((e & 2) ? 8 : 0);
+            const int tok = 8 * t + 2 * tq + (e & 1);
+            if (n >= op.N || tok >= op.M) return;
+            float f = __int2float_rn(acc);
+            f = __fmul_rn(f, sa_reg[t][e & 1]);
+            f = __fmul_rn(f, sw[(e & 2) ? 1 : 0]);
+            const uint16_t b = __bfloat16_as_ushort(__float2bfloat16_rn(f));
+            if (op.y) op.y[static_cast<size_t>(tok) * op.N + n] = b;
+            if (head) {
+                const unsigned long long key = argmax_key(b, n);
+                if (key > best[t][e & 1]) best[t][e & 1] = key;
             }
         };
+        auto slot_of = [&](int rb) {
+            const int slot = unit_owner(static_cast<long long>(rb) * op.upr, op.units, G);
+            return ws.partial + static_cast<size_t>(slot) * (kBM * kMaxTok);
+        };
+        auto elem = [&](int t, int e) { return (rg * 16 + g + ((e & 2) ? 8 : 0)) * kMaxTok + 8 * t + 2 * tq + (e & 1); };
+        // Add a run's partial sums (nch of the row block's upr K units) to the
+        // row block's slot; old[] receives the values before the add.
+        auto push = [&](int rb, int nch, const int32_t (&v)[MT][4], unsigned long long (&old)[MT][4]) {
+            unsigned long long *part = slot_of(rb);
+            const unsigned long long tag = static_cast<unsigned long long>(nch) << 40;
+#pragma unroll
+            for (int t = 0; t < MT; ++t)
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    old[t][e] = atomicAdd(&part[elem(t, e)],
+                                          tag + static_cast<unsigned long long>(static_cast<long long>(v[t][e])));
+        };
+        // The add that brought an element's unit count to upr completed it:
+        // its issuer, seeing the slot's value just after its own add, holds
+        // the whole sum; it writes the output and clears the slot.
+        auto finish1 = [&](int rb, int t, int e, unsigned long long after, const float (&sw)[2]) {
+            const long long a = static_cast<long long>(after);
+            const long long units = (a + (1LL << 39)) >> 40;
+            if (units == op.upr) {
+                slot_of(rb)[elem(t, e)] = 0ull;
+                emit1(rb, t, e, static_cast<int32_t>(a - (units << 40)), sw);
+            }
+        };
+        auto after_add = [&](int nch, int32_t v, unsigned long long old) {
+            return old + (static_cast<unsigned long long>(nch) << 40) +
+                   static_cast<unsigned long long>(static_cast<long long>(v));
+        };
 
-        int pend_rb[2] = {0, 0}, pend_n[2] = {0, 0};
-        int npend = 0;
+        // The first run of the range, if it shares its row block with earlier
+        // CTAs, is completed only after the last run is pushed, so that the
+        // two atomic round trips overlap.
+        bool first_deferred = false;
+        int f_rb = 0;
+        float f_sw[2] = {0.0f, 0.0f};
+        unsigned long long *my_defer = sdefer + (rg * 32 + lane) * (MT * 4);
         long long u = u_begin;
         while (u < u_end) {
             const int rb = static_cast<int>(u / op.upr);
@@ -519,61 +557,39 @@ __global__ void __launch_bounds__(kThreads, 2) program_kernel(const ProgHeader *
                                             2 * tq + (e & 1)];
             }
             consumer_bar();
-            if (c0 == 0 && nch == op.upr) {
-                if (!*abort_flag && kq == 0) epilogue(rb, v, sw);
-            } else {
-                if (!*abort_flag && kq == 0) {
-                    const int slot = unit_owner(static_cast<long long>(rb) * op.upr, op.units, G);
-                    int32_t *part = ws.partial + static_cast<size_t>(slot) * (kBM * kMaxTok);
+            if (kq == 0 && !*abort_flag) {
+                if (c0 == 0 && nch == op.upr) {
 #pragma unroll
                     for (int t = 0; t < MT; ++t)
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int r = rg * 16 + g + ((e & 2) ? 8 : 0);
-                            const int tok = 8 * t + 2 * tq + (e & 1);
-                            if (v[t][e] != 0) atomicAdd(&part[r * kMaxTok + tok], v[t][e]);
-                        }
+                        for (int e = 0; e < 4; ++e) emit1(rb, t, e, v[t][e], sw);
+                } else {
+                    unsigned long long old[MT][4];
+                    push(rb, nch, v, old);
+                    if (u == u_begin && u + nch < u_end) {
+                        first_deferred = true;
+                        f_rb = rb;
+                        f_sw[0] = sw[0];
+                        f_sw[1] = sw[1];
+#pragma unroll
+                        for (int t = 0; t < MT; ++t)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) my_defer[t * 4 + e] = after_add(nch, v[t][e], old[t][e]);
+                    } else {
+#pragma unroll
+                        for (int t = 0; t < MT; ++t)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) finish1(rb, t, e, after_add(nch, v[t][e], old[t][e]), sw);
+                    }
                 }
-                pend_rb[npend] = rb;
-                pend_n[npend] = nch;
-                ++npend;
             }
             u += nch;
         }
-        // settle row blocks shared with neighbouring CTAs (last contributor finishes)
-        if (npend > 0) {
-            consumer_bar();
-            if (ctid == 0) {
-                for (int k = 0; k < npend; ++k) {
-                    int last = 0;
-                    if (!*abort_flag) {
-                        const int slot = unit_owner(static_cast<long long>(pend_rb[k]) * op.upr, op.units, G);
-                        const int old = atom_add_acq_rel_gpu(&ws.rb_counter[slot], pend_n[k]);
-                        last = (old + pend_n[k] == op.upr);
-                        if (last) atomicExch(&ws.rb_counter[slot], 0);
-                    }
-                    last_flag[k] = last;
-                }
-            }
-            consumer_bar();
-            for (int k = 0; k < npend; ++k) {
-                if (!last_flag[k] || kq != 0) continue;
-                const int slot = unit_owner(static_cast<long long>(pend_rb[k]) * op.upr, op.units, G);
-                int32_t *part = ws.partial + static_cast<size_t>(slot) * (kBM * kMaxTok);
-                int32_t v[MT][4];
+        if (first_deferred && !*abort_flag) {
 #pragma unroll
-                for (int t = 0; t < MT; ++t)
+            for (int t = 0; t < MT; ++t)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int r = rg * 16 + g + ((e & 2) ? 8 : 0);
-                        const int tok = 8 * t + 2 * tq + (e & 1);
-                        v[t][e] = atomicExch(&part[r * kMaxTok + tok], 0);
-                    }
-                float swp[2];
-                load_sw(pend_rb[k], swp);
-                epilogue(pend_rb[k], v, swp);
-            }
-            consumer_bar();
+                for (int e = 0; e < 4; ++e) finish1(f_rb, t, e, my_defer[t * 4 + e], f_sw);
         }
         if (head) {
 #pragma unroll
@@ -655,9 +671,8 @@ cudaError_t launch_program(const void *prog, void *wsp, int grid, cudaStream_t s
     ws.bar = reinterpret_cast<int *>(b + 8);
     ws.exit_ticket = reinterpret_cast<int *>(b + 12);
     ws.qdone = reinterpret_cast<int *>(b + 16);
-    ws.rb_counter = reinterpret_cast<int32_t *>(b + kPwCounterOff);
     ws.best = reinterpret_cast<unsigned long long *>(b + kPwBestOff);
-    ws.partial = reinterpret_cast<int32_t *>(b + kPwPartialOff);
+    ws.partial = reinterpret_cast<unsigned long long *>(b + kPwPartialOff);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(kThreads);

@@ -22,11 +22,23 @@ namespace bi {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// fp32 -> bf16 bit pattern, round to nearest, ties to even, in integer
+// arithmetic (conversion instructions issue at a fraction of the ALU rate).
+// Adding 0x7FFF plus the pattern's lowest kept bit carries into the kept half
+// exactly when the dropped half is above the midpoint, or at it with an odd
+// kept half; a carry out of the significand moves to the next binade or to
+// infinity, as IEEE rounding does.  NaN gives 0x7FC0 (never produced here:
+// the steps see finite values only).
+__device__ __forceinline__ uint32_t bf16_rne_bits(float f)
+{
+    const uint32_t u = __float_as_uint(f);
+    const uint32_t r = (u + 0x7FFFu + ((u >> 16) & 1u)) >> 16;
+    return (u & 0x7FFFFFFFu) > 0x7F800000u ? 0x7FC0u : r;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 {
-    const uint32_t a = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
-    const uint32_t b = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
-    return a | (b << 16);
+    return bf16_rne_bits(lo) | (bf16_rne_bits(hi) << 16);
 }
 
 __device__ __forceinline__ float absmax8(const uint4 &t, float amax)
@@ -104,6 +116,17 @@ __device__ __forceinline__ uint4 rescale8(const uint4 &t, int p)
     uint32_t o[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) o[e] = pack_bf16x2(scale_pow2(bf16_lo(a[e]), p), scale_pow2(bf16_hi(a[e]), p));
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// bf16_rne(t * f) elementwise for an exact power of two f (a normal or
+// subnormal fp32 value): the form of rescale8 for shifts p <= 127.
+__device__ __forceinline__ uint4 scale8(const uint4 &t, float f)
+{
+    const uint32_t a[4] = {t.x, t.y, t.z, t.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) o[e] = pack_bf16x2(__fmul_rn(bf16_lo(a[e]), f), __fmul_rn(bf16_hi(a[e]), f));
     return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
