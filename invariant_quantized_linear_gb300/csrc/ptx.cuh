@@ -201,10 +201,11 @@ __device__ __forceinline__ void i8x4_to_f16x2x2(uint32_t v, uint32_t &lo, uint32
 // quotient fl(v / s) by less than 3 * 2^-24 * 127.0001 < 2.3e-5 (three
 // roundings of relative size <= 2^-24 each), so both round to the same
 // integer unless the product lies within that distance of a half-integer.
-// Products within 2^-10 of a half-integer take the exact division instead.
+// Products within 2^-15 (3.05e-5) of a half-integer take the exact division
+// instead, about one element in sixteen thousand.
 // The exact path is one out-of-line copy: inlined at every element it would
 // multiply the code of an unrolled row loop for a branch taken about once in
-// five hundred elements.
+// sixteen thousand elements.
 static __device__ __noinline__ int quant_code_exact(float v, float s)
 {
     return __float2int_rn(__fdiv_rn(v, s));
@@ -224,7 +225,7 @@ __device__ __forceinline__ int quant_code(float v, float s, float r)
     const float d = fabsf(__fsub_rn(t, kf));   // exact: |t| < 2^8
     int k = __float_as_int(u) - 0x4B400000;
     // (also taken when r overflowed for a tiny subnormal s: t is then inf or NaN)
-    if (!(d < 0.5f - 0.0009765625f)) k = quant_code_exact(v, s);
+    if (!(d < 0.5f - 0x1p-15f)) k = quant_code_exact(v, s);
     return max(-127, min(127, k));
 }
 
