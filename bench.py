@@ -300,9 +300,51 @@ class Stack:
         return sum(self.op_bytes(o) for o in self.ops(M) if o.kind == bi.BI_OP_LINEAR)
 
 
+def prefill_measure(bi, torch, st, stream, peaks):
+    """The prefill contraction (M = 512 and 2048 tokens, K = 4096, N = 12288:
+    layer 0's gate projection) through bi_linear_w8a8, timed alone: int
+    operations per second against the measured dense bf16 tensor peak (the
+    kernel runs the int8 products on the f16 tensor-core MMA)."""
+    import gen
+    out = {}
+    K, N = 4096, 12288
+    wq = st.W[0]["gu"][0][:N]
+    sw = st.W[0]["gu"][1][:N]
+    for Mp in (512, 2048):
+        x = torch.from_numpy(gen.activations(gen.PREFILL, Mp, K).view(np.int16)).to(st.dev)
+        q = torch.empty((Mp, K), dtype=torch.int8, device=st.dev)
+        s = torch.empty(Mp, dtype=torch.float32, device=st.dev)
+        y = torch.empty((Mp, N), dtype=torch.int16, device=st.dev)
+        ws = bi.new_workspace(Mp, N, K, device=st.dev)
+        with torch.cuda.stream(stream):
+            bi.bi_quantize_act(x, q, s)
+            for _ in range(3):
+                bi.bi_linear_w8a8(q, s, wq, sw, y, ws)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            reps = 20
+            e0.record(stream)
+            for _ in range(reps):
+                bi.bi_linear_w8a8(q, s, wq, sw, y, ws)
+            e1.record(stream)
+        stream.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        tops = 2.0 * Mp * N * K / (ms * 1e-3) / 1e12
+        out[str(Mp)] = {"ms": round(ms, 4), "tops": round(tops, 1),
+                        "frac_of_bf16_peak": round(tops / float(peaks["bf16_tflops"]), 4)}
+    out["note"] = ("y = W8A8(x) with K=4096, N=12288 (int8 x int8 -> exact int32 via f16 mma.sync); "
+                   "peak = measured cuBLAS dense bf16 (tcgen05), which sm_103a offers no int8 counterpart of")
+    return out
+
+
 def source_sha(path):
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()
+    """Hash of a kernel's source and the headers it is built from."""
+    h = hashlib.sha256()
+    d = os.path.dirname(path)
+    for name in [os.path.basename(path), "ptx.cuh", "stream_mma.cuh", "row_ops.cuh", "kernels.cuh"]:
+        with open(os.path.join(d, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
 
 
 def run_ours(args):
@@ -442,6 +484,7 @@ def run_ours(args):
     if NCU_TRAFFIC["source_sha256"] == source_sha(src):
         traffic = NCU_TRAFFIC["bytes_per_launch"]
 
+    prefill = prefill_measure(bi, torch, st, stream, peaks) if not args.no_sweep else None
     cpu = cpu_baseline(bounded_s=12.0) if rank == 0 else None
     if rank == 0:
         line = {
@@ -474,6 +517,7 @@ def run_ours(args):
             "gpu_launches": st.launches_per_step(args.mode) * args.steps,
             "clocks": clk,
             "cpu_baseline": cpu,
+            "prefill": prefill,
             "setup_s": round(setup_s, 1),
         }
         print(json.dumps(line), flush=True)

@@ -206,6 +206,16 @@ BI_API bi_status bi_lmhead_argmax(const int8_t *q, const float *s_a, int M, int 
 BI_API bi_status bi_workspace_status(void *ws, size_t ws_bytes, bi_stream_t stream);
 
 /*
+ * Test of the failure path: launches one thread that waits, with the same
+ * bounded wait the kernels use, on a barrier phase that nothing completes.
+ * After the wait limit (2 s of GPU time) it gives up and sets the status
+ * word of `ws` (a linear workspace, >= bi_linear_workspace_size(1, 1, 16)
+ * bytes), so that bi_workspace_status then returns BI_ERR_TIMEOUT.  Nothing
+ * faults or hangs; the context stays usable.
+ */
+BI_API bi_status bi_selftest_wait_timeout(void *ws, size_t ws_bytes, bi_stream_t stream);
+
+/*
  * Verify-pass executor: a program of ops run by one persistent kernel.
  *
  * A decode or verify pass is a chain of small dependent steps (quantise an

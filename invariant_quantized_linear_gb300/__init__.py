@@ -46,6 +46,8 @@ lib.bi_linear_w8a8.argtypes = [_vp, _vp, _ci, _ci, _vp, _vp, _ci, _vp, _vp, _sz,
 lib.bi_linear_w8a8.restype = _ci
 lib.bi_lmhead_argmax.argtypes = [_vp, _vp, _ci, _ci, _vp, _vp, _ci, _vp, _vp, _vp, _sz, _cu, _vp]
 lib.bi_lmhead_argmax.restype = _ci
+lib.bi_selftest_wait_timeout.argtypes = [_vp, _sz, _vp]
+lib.bi_selftest_wait_timeout.restype = _ci
 lib.bi_workspace_status.argtypes = [_vp, _sz, _vp]
 lib.bi_workspace_status.restype = _ci
 lib.bi_linear_w8a8_noalloc.argtypes = [_vp, _vp, _ci, _ci, _vp, _vp, _ci, _vp, _cu, _vp]
@@ -249,6 +251,13 @@ def new_program(n_ops: int, device="cuda") -> torch.Tensor:
     buf = torch.empty(n + 128, dtype=torch.uint8, device=device)
     off = (-buf.data_ptr()) % 128
     return buf[off:off + n]
+
+
+def bi_selftest_wait_timeout(ws: torch.Tensor, stream=None) -> None:
+    """Launch a bounded wait that nothing satisfies (about 2 s); the workspace
+    status then reads BI_ERR_TIMEOUT."""
+    _check(lib.bi_selftest_wait_timeout(_ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
+           "bi_selftest_wait_timeout")
 
 
 def bi_workspace_status(ws: torch.Tensor, stream=None) -> int:

@@ -290,6 +290,14 @@ bi_status bi_lmhead_argmax(const int8_t *q, const float *s_a, int M, int K, cons
     return run_skinny(q, s_a, M, K, w_q, s_w, N, logits, argmax, ws, flags, stream);
 }
 
+bi_status bi_selftest_wait_timeout(void *ws, size_t ws_bytes, bi_stream_t stream)
+{
+    if (!ws || ws_bytes < bi::kWsBytes || !aligned4(ws)) return BI_ERR_WORKSPACE;
+    const bi_status st = device_info(nullptr);
+    if (st != BI_OK) return st;
+    return from_cuda(bi::launch_wait_selftest(static_cast<int *>(ws), stream));
+}
+
 bi_status bi_workspace_status(void *ws, size_t ws_bytes, bi_stream_t stream)
 {
     if (!ws || ws_bytes < bi::kWsBytes) return BI_ERR_WORKSPACE;

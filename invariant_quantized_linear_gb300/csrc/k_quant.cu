@@ -313,6 +313,19 @@ __global__ void __launch_bounds__(kQuantThreads) requant_pow2_kernel(const int8_
     if (threadIdx.x == 0) s_w_out[row] = s_new;
 }
 
+// One thread waits, with the library's bounded wait, on a barrier phase that
+// nothing will complete; when the wait gives up it reports a timeout in the
+// status word, as the linear and program kernels do.
+__global__ void wait_selftest_kernel(int *status)
+{
+    __shared__ uint64_t bar;
+    __shared__ int never;
+    mbar_init(&bar, 1);
+    never = 0;
+    fence_mbarrier_init();
+    if (!mbar_wait_bounded(&bar, 0, &never)) atomicExch(status, DEV_TIMEOUT);
+}
+
 }  // namespace
 
 cudaError_t launch_quantize_act(const uint16_t *x, int64_t ldx, int M, int K, int8_t *q, float *s_a, bool pdl,
@@ -334,6 +347,12 @@ cudaError_t launch_relu_mul_quantize(const uint16_t *gu, int64_t ldgu, int M, in
 {
     const RowArgs a = {gu, ldgu, m_out, K, q, s_a};
     return launch_rows<kRowReluMul>(a, M, pdl, stream);
+}
+
+cudaError_t launch_wait_selftest(int *status, cudaStream_t stream)
+{
+    wait_selftest_kernel<<<1, 1, 0, stream>>>(status);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_quantize_weight(const float *w, int64_t ldw, int N, int K, int8_t *w_q, float *s_w,

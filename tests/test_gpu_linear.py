@@ -147,3 +147,21 @@ def test_packed_weights_equal_separate_calls(bi):
     packed = linear(bi, q, s, wq, sw, flags=bi.BI_FLAG_PDL)
     sep = torch.cat([linear(bi, q, s, w, v) for w, v in parts], dim=1)
     assert torch.equal(packed, sep)
+
+
+def test_bounded_wait_reports_timeout_and_context_survives(bi):
+    """A wait that nothing satisfies gives up after its limit and reports
+    BI_ERR_TIMEOUT through the workspace; later work on the same context runs
+    normally (no fault, no hang)."""
+    ws = bi.new_workspace(1, 1, 16)
+    bi.bi_selftest_wait_timeout(ws)
+    assert bi.bi_workspace_status(ws) == bi.BI_ERR_TIMEOUT
+    assert bi.bi_workspace_status(ws) == bi.BI_OK          # the status word was cleared
+    x = gen.act_bf16(5, 1, 2, 256)
+    q, s = quant_act(bi, x)
+    wq, sw = weights(bi, gen.weight_f32(5, 0, 0, 64, 256), True)
+    y = linear(bi, q, s, wq, sw, ws=ws)
+    q_o, s_o = oracle.quantize_act(x)
+    wq_o, sw_o = oracle_weights(oracle, gen.weight_f32(5, 0, 0, 64, 256), True)
+    assert np.array_equal(to_np(y), oracle.linear_w8a8(q_o, s_o, wq_o, sw_o))
+    assert bi.bi_workspace_status(ws) == bi.BI_OK
