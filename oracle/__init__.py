@@ -42,6 +42,8 @@ def lib():
         L.oracle_residual_rescale.restype = None
         L.oracle_relu_mul.argtypes = [vp, i64, ci, ci, vp]
         L.oracle_relu_mul.restype = None
+        L.oracle_greedy_verify.argtypes = [vp, vp, ci, vp]
+        L.oracle_greedy_verify.restype = None
         L.oracle_num_threads.argtypes = []
         L.oracle_num_threads.restype = ci
         _LIB = L
@@ -195,6 +197,18 @@ def verify_pass(h0: np.ndarray, layers, head, q_rows: int, record: bool = False)
     q, s = quantize_act(h)
     am, _ = lmhead_argmax(q, s, *head, want_logits=False)
     return am, h, recs
+
+
+def greedy_verify(argmax: np.ndarray, draft: np.ndarray):
+    """(accepted count L, next token) for the argmax rows [M] of a verify pass
+    whose inputs after the first were the drafted tokens draft [M - 1]."""
+    am = _c(argmax, np.int32)
+    M = am.shape[0]
+    d = _c(draft if len(draft) else np.zeros(1, np.int32), np.int32)
+    assert len(draft) == M - 1
+    out = np.empty(2, np.int32)
+    lib().oracle_greedy_verify(am.ctypes.data, d.ctypes.data, M, out.ctypes.data)
+    return int(out[0]), int(out[1])
 
 
 def num_threads() -> int:

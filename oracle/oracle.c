@@ -316,6 +316,27 @@ void oracle_relu_mul(const uint16_t *gu, int64_t ld, int M, int K, uint16_t *out
     }
 }
 
+/* ------------------------------------------------------- greedy verification
+ *
+ * Greedy speculative decoding keeps exactly the tokens plain greedy decoding
+ * would produce ([cintu] introduction; [goyal] "Speculative decoding (SD)"):
+ * the verify pass runs the target on the last accepted token followed by the
+ * M - 1 drafted tokens d_1 .. d_{M-1}; row i's argmax a_i is the target's
+ * choice for the token after input i.  Drafted token d_{i+1} is accepted
+ * while it equals a_i, so the accepted count L is the length of the longest
+ * prefix with a_i == d_{i+1} (0 <= L <= M - 1), and the next token is a_L
+ * (the correction after a rejection, or the bonus token when every draft is
+ * accepted).  out[0] = L, out[1] = a_L.
+ */
+void oracle_greedy_verify(const int32_t *argmax, const int32_t *draft, int M, int32_t *out)
+{
+    int L = 0;
+    while (L < M - 1 && argmax[L] == draft[L])
+        ++L;
+    out[0] = L;
+    out[1] = argmax[L];
+}
+
 /* Number of OpenMP threads the parallel loops above use (1 without OpenMP). */
 int oracle_num_threads(void)
 {

@@ -580,3 +580,38 @@ def test_verify_pass_rows_are_batch_invariant():
         for a, b in zip(recs, recs1):
             for k in a:
                 assert np.array_equal(a[k][r], b[k][0]), k
+
+
+# --------------------------------------------------------------- greedy verify
+
+def _plain_greedy_accept(argmax, draft):
+    """Restatement from the definition: step through the drafts one position
+    at a time, as plain greedy decoding would emit tokens."""
+    emitted = []
+    for i in range(len(argmax)):
+        emitted.append(int(argmax[i]))
+        if i == len(draft) or int(draft[i]) != int(argmax[i]):
+            return i, emitted[-1]
+    raise AssertionError
+
+
+@pytest.mark.parametrize("M", [1, 2, 5, 8, 16])
+def test_greedy_verify_against_step_by_step_restatement(M):
+    rng = np.random.default_rng(90 + M)
+    for trial in range(200):
+        am = rng.integers(0, 6, M).astype(np.int32)      # a small vocabulary makes matches common
+        dr = am[:M - 1].copy()
+        cut = rng.integers(0, M)
+        if cut < M - 1:
+            dr[cut] = (dr[cut] + 1 + rng.integers(0, 4)) % 6
+        got = oracle.greedy_verify(am, dr)
+        assert got == _plain_greedy_accept(am, dr), (trial, am, dr)
+        L, tok = got
+        assert 0 <= L <= M - 1 and tok == am[L]
+        assert all(am[i] == dr[i] for i in range(L))
+
+
+def test_greedy_verify_edge_cases():
+    assert oracle.greedy_verify(np.array([7], np.int32), np.array([], np.int32)) == (0, 7)       # decode: no drafts
+    assert oracle.greedy_verify(np.array([3, 4, 5], np.int32), np.array([3, 4], np.int32)) == (2, 5)  # all accepted
+    assert oracle.greedy_verify(np.array([3, 4, 5], np.int32), np.array([9, 4], np.int32)) == (0, 3)  # first rejected
