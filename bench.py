@@ -1,14 +1,16 @@
 #!/usr/bin/env python3
 """Benchmark: one chained verify pass of a 36-layer Qwen3-8B-shaped W8A8 stack.
 
-A step is one pass of the whole hot path over one batch of M tokens: the
+A step is one pass of the whole hot path over one batch of M tokens (the last
+accepted token and M - 1 drafted ones): the
 residual stream h (bf16 [M, 4096]) runs through 36 layers, each
     y_qkv = linear(quant(h), W_qkv)          q, k, v packed (6144 rows)
     y_o   = linear(quant(y_qkv[:, :4096]), W_o)   (q slice: attention stand-in)
     h     = rescale(bf16(h + y_o));  y_gu = linear(quant(h), W_gu)   gate, up packed
     y_d   = linear(quant(bf16(relu(gate) * up)), W_down)
     h     = rescale(bf16(h + y_d))
-and then the LM head's greedy argmax over 151,936 rows.  Every quantisation is
+and then the LM head's greedy argmax over 151,936 rows with the greedy
+verification of the drafts (accepted count and next token).  Every quantisation is
 fused with the elementwise step before it.  Weights (7,568,097,280 bytes of
 int8 plus power-of-two scales) come from the seeded recipe, are quantised on
 the GPU and stay resident; the step reads all of them, far more than the L2
@@ -205,6 +207,9 @@ class Stack:
             self.q[name] = t.empty((M16, K), dtype=t.int8, device=device)
             self.s[name] = t.empty(M16, dtype=t.float32, device=device)
         self.argmax = t.empty(M16, dtype=t.int32, device=device)
+        # drafted tokens of the verify pass (synthetic) and the verification result
+        self.draft = t.from_numpy(gen.u64(wl.seed, 11, M16).astype(np.int64) % self.V).to(t.int32).to(device)
+        self.accept = t.zeros(2, dtype=t.int32, device=device)
         self.ws = bi.new_workspace(M16, self.V, self.I, device=device)
         torch.cuda.synchronize()
 
@@ -235,7 +240,8 @@ class Stack:
                     bi.op_relu_mul_quant(y["gu"][:M], self.I, q["down"][:M], s["down"][:M]),
                     bi.op_linear(q["down"][:M], s["down"][:M], *W["down"], y["down"][:M]),
                     bi.op_residual_quant(h, y["down"][:M], q[nxt][:M], s[nxt][:M])]
-        ops.append(bi.op_lmhead(q["head"][:M], s["head"][:M], *self.head, None, self.argmax[:M]))
+        ops.append(bi.op_lmhead(q["head"][:M], s["head"][:M], *self.head, None, self.argmax[:M],
+                                draft=self.draft[:M - 1] if M > 1 else None, accept=self.accept))
         return ops
 
     def build_program(self, M):
@@ -272,9 +278,10 @@ class Stack:
         if not linears_only:
             bi.bi_lmhead_argmax(q["head"][:M], s["head"][:M], *self.head, None, self.argmax[:M], ws,
                                 flags=flags)
+            bi.bi_greedy_verify(self.argmax[:M], self.draft[:M - 1] if M > 1 else None, self.accept)
 
     def launches_per_step(self, mode):
-        return 1 if mode == "program" else 2 + 8 * self.layers
+        return 2 if mode == "program" else 3 + 8 * self.layers
 
     def op_bytes(self, op):
         """Algorithmic bytes of one op: what it must read and write."""
@@ -289,7 +296,7 @@ class Stack:
         tot = N * K + 4 * N + M * K + 4 * M
         if op.kind == bi.BI_OP_LINEAR:
             return tot + 2 * M * N
-        return tot + 4 * M + (2 * M * N if op.y else 0)
+        return tot + 4 * M + (2 * M * N if op.y else 0) + (4 * (M - 1) + 8 if op.accept else 0)
 
     def step_bytes(self, M):
         """Algorithmic bytes of one step: the input copy and every op."""
@@ -460,6 +467,7 @@ def run_ours(args):
     # end to end: the input rows H2D from pinned memory, the step's graph, argmax D2H
     host_h0 = torch.from_numpy(st.h0_np.view(np.int16)).pin_memory()
     host_am = torch.empty(16, dtype=torch.int32).pin_memory()
+    host_acc = torch.empty(2, dtype=torch.int32).pin_memory()
     h2d = int(host_h0[:M].numel()) * 2
     e2e_steps = max(3, args.steps // 2)
     barrier()
@@ -471,6 +479,7 @@ def run_ours(args):
             st.h0[:M].copy_(host_h0[:M], non_blocking=True)
             g.replay()
             host_am[:M].copy_(st.argmax[:M], non_blocking=True)
+            host_acc.copy_(st.accept, non_blocking=True)
         e1.record(stream)
     barrier()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
@@ -499,9 +508,10 @@ def run_ours(args):
                        "activations": ("chained: residual stream through 36 layers (q slice of q/k/v as the "
                                        "attention stand-in, ReLU-gated MLP, power-of-two row rescale)"),
                        "packing": "q/k/v and gate/up weight rows packed: one call per group",
+                       "verify": "greedy verification of M - 1 synthetic drafted tokens fused into the LM head",
                        "launch": ("one verify-pass program launch per step (persistent cooperative kernel, "
-                                  "grid barrier between ops) after a device copy of the input rows, in a CUDA "
-                                  "graph" if args.mode == "program" else
+                                  "grid barrier between ops) after a device copy of the input rows, then a "
+                                  "one-warp greedy-verify kernel, in a CUDA graph" if args.mode == "program" else
                                   "CUDA graph of the step, one launch per op, programmatic dependent launch"),
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "pct_of_hbm_copy": round(100 * gbs / world / peak, 1),
@@ -513,7 +523,7 @@ def run_ours(args):
                          "launch_us": round(lin_ms * 1e3 / lin_launches, 3),
                          "peak_kind": kind, "note": note},
             "e2e": {"value": round(e2e_gbs, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": 4 * M, "ms_per_step": round(e2e_ms, 4)},
+                    "d2h_bytes_per_step": 4 * M + 8, "ms_per_step": round(e2e_ms, 4)},
             "gpu_launches": st.launches_per_step(args.mode) * args.steps,
             "clocks": clk,
             "cpu_baseline": cpu,

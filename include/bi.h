@@ -206,6 +206,24 @@ BI_API bi_status bi_lmhead_argmax(const int8_t *q, const float *s_a, int M, int 
 BI_API bi_status bi_workspace_status(void *ws, size_t ws_bytes, bi_stream_t stream);
 
 /*
+ * Greedy verification of a verify pass, the step after the LM head.  Greedy
+ * speculative decoding keeps exactly the tokens plain greedy decoding would
+ * produce ("why speculative decoding changed my output", introduction; "My
+ * speculative decoder got slower", "Speculative decoding (SD)").  The pass
+ * ran the target on the last accepted token followed by the drafted tokens
+ * d_1 .. d_{M-1}; argmax[i] is the target's choice after input i.
+ *   argmax int32 [M] (from bi_lmhead_argmax), draft int32 [M - 1] (NULL when
+ *   M == 1), out int32 [2] receives L = the length of the longest prefix with
+ *   argmax[i] == draft[i], and argmax[L] (the correction, or the bonus token
+ *   when all M - 1 drafts are accepted).  Device pointers, 4-byte aligned.
+ * One warp; M <= 65535.  In a program, the same result is produced by an
+ * LM-head op whose `draft` and `accept` fields are set, in the CTA that
+ * finishes the argmax.
+ */
+BI_API bi_status bi_greedy_verify(const int32_t *argmax, const int32_t *draft, int M, int32_t *out,
+                                  bi_stream_t stream);
+
+/*
  * Test of the failure path: launches one thread that waits, with the same
  * bounded wait the kernels use, on a barrier phase that nothing completes.
  * After the wait limit (2 s of GPU time) it gives up and sets the status
@@ -263,6 +281,8 @@ typedef struct {
     uint16_t *y;            /* linear: output [M, N]; head: logits or NULL;
                                residual: the stream h; relu-mul: m or NULL */
     int32_t *argmax;        /* head: output [M] */
+    const int32_t *draft;   /* head, optional: drafted tokens [M - 1] (see bi_greedy_verify) */
+    int32_t *accept;        /* head, optional: [2] accepted count and next token, or NULL */
 } bi_op;
 
 BI_API size_t bi_program_bytes(int n_ops);

@@ -46,6 +46,8 @@ lib.bi_linear_w8a8.argtypes = [_vp, _vp, _ci, _ci, _vp, _vp, _ci, _vp, _vp, _sz,
 lib.bi_linear_w8a8.restype = _ci
 lib.bi_lmhead_argmax.argtypes = [_vp, _vp, _ci, _ci, _vp, _vp, _ci, _vp, _vp, _vp, _sz, _cu, _vp]
 lib.bi_lmhead_argmax.restype = _ci
+lib.bi_greedy_verify.argtypes = [_vp, _vp, _ci, _vp, _vp]
+lib.bi_greedy_verify.restype = _ci
 lib.bi_selftest_wait_timeout.argtypes = [_vp, _sz, _vp]
 lib.bi_selftest_wait_timeout.restype = _ci
 lib.bi_workspace_status.argtypes = [_vp, _sz, _vp]
@@ -63,7 +65,8 @@ class bi_op(ctypes.Structure):
     """One op of a verify-pass program (struct bi_op of include/bi.h)."""
     _fields_ = [("kind", _ci), ("M", _ci), ("N", _ci), ("K", _ci),
                 ("x", _vp), ("ldx", _i64), ("q", _vp), ("s_a", _vp),
-                ("w_q", _vp), ("s_w", _vp), ("y", _vp), ("argmax", _vp)]
+                ("w_q", _vp), ("s_w", _vp), ("y", _vp), ("argmax", _vp),
+                ("draft", _vp), ("accept", _vp)]
 
 
 lib.bi_program_build.argtypes = [ctypes.POINTER(bi_op), _ci, _vp, _sz]
@@ -239,10 +242,12 @@ def op_linear(q: torch.Tensor, s_a: torch.Tensor, w_q: torch.Tensor, s_w: torch.
 
 
 def op_lmhead(q: torch.Tensor, s_a: torch.Tensor, w_q: torch.Tensor, s_w: torch.Tensor,
-              logits: torch.Tensor | None, argmax: torch.Tensor) -> bi_op:
+              logits: torch.Tensor | None, argmax: torch.Tensor, draft: torch.Tensor | None = None,
+              accept: torch.Tensor | None = None) -> bi_op:
+    """LM head; with `accept` (int32 [2]) also greedy verification against `draft` (int32 [M - 1])."""
     M, K = q.shape
     return bi_op(BI_OP_LMHEAD, M, w_q.shape[0], K, None, 0, _ptr(q), _ptr(s_a), _ptr(w_q), _ptr(s_w),
-                 _ptr(logits), _ptr(argmax))
+                 _ptr(logits), _ptr(argmax), _ptr(draft), _ptr(accept))
 
 
 def new_program(n_ops: int, device="cuda") -> torch.Tensor:
@@ -251,6 +256,13 @@ def new_program(n_ops: int, device="cuda") -> torch.Tensor:
     buf = torch.empty(n + 128, dtype=torch.uint8, device=device)
     off = (-buf.data_ptr()) % 128
     return buf[off:off + n]
+
+
+def bi_greedy_verify(argmax: torch.Tensor, draft: torch.Tensor | None, out: torch.Tensor, stream=None) -> None:
+    """argmax int32 [M], draft int32 [M - 1] (or None when M == 1), out int32 [2]:
+    accepted draft count and next token."""
+    _check(lib.bi_greedy_verify(_ptr(argmax), _ptr(draft), argmax.shape[0], _ptr(out), _stream(stream)),
+           "bi_greedy_verify")
 
 
 def bi_selftest_wait_timeout(ws: torch.Tensor, stream=None) -> None:

@@ -290,6 +290,15 @@ bi_status bi_lmhead_argmax(const int8_t *q, const float *s_a, int M, int K, cons
     return run_skinny(q, s_a, M, K, w_q, s_w, N, logits, argmax, ws, flags, stream);
 }
 
+bi_status bi_greedy_verify(const int32_t *argmax, const int32_t *draft, int M, int32_t *out, bi_stream_t stream)
+{
+    if (!argmax || !out || M < 1 || M > 65535 || (M > 1 && !draft)) return BI_ERR_INVALID_ARG;
+    if (!aligned4(argmax) || !aligned4(out) || (draft && !aligned4(draft))) return BI_ERR_ALIGNMENT;
+    const bi_status st = device_info(nullptr);
+    if (st != BI_OK) return st;
+    return from_cuda(bi::launch_greedy_verify(argmax, draft, M, out, stream));
+}
+
 bi_status bi_selftest_wait_timeout(void *ws, size_t ws_bytes, bi_stream_t stream)
 {
     if (!ws || ws_bytes < bi::kWsBytes || !aligned4(ws)) return BI_ERR_WORKSPACE;

@@ -64,6 +64,12 @@ struct alignas(128) ProgHeader {
     int n_maps;
     int mt;              // token tiles: 1 (M <= 8) or 2 (M <= 16)
     int magic;
+    // greedy verification after the run, for the last LM-head op that asks for
+    // it (verify_M = 0: none): its argmax, drafted tokens and result
+    int verify_M;
+    const int32_t *verify_argmax;
+    const int32_t *verify_draft;
+    int32_t *verify_accept;
 };
 
 constexpr int kProgMagic = 0x42495031;  // "BIP1"
@@ -634,6 +640,7 @@ __global__ void __launch_bounds__(kThreads, 2) program_kernel(const ProgHeader *
                         op.argmax[lane] =
                             static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(vv & 0xFFFFFFFFull));
                     }
+
                     if (lane == 0) atomicExch(ws.ticket, 0);
                 }
             }
@@ -650,6 +657,30 @@ __global__ void __launch_bounds__(kThreads, 2) program_kernel(const ProgHeader *
             atomicExch(ws.qdone, 0);
             atomicExch(ws.exit_ticket, 0);
         }
+    }
+}
+
+// Greedy verification after a program run (the same computation as
+// bi_greedy_verify), one warp; nothing to do for a program without it.
+__global__ void program_verify_kernel(const ProgHeader *__restrict__ prog)
+{
+    const int M = prog->verify_M;
+    if (M < 1) return;
+    const int32_t *argmax = prog->verify_argmax, *draft = prog->verify_draft;
+    const int lane = threadIdx.x;
+    int L = M - 1;
+    for (int base = 0; base < M - 1; base += 32) {
+        const int i = base + lane;
+        const bool miss = i < M - 1 && argmax[i] != draft[i];
+        const unsigned b = __ballot_sync(0xffffffffu, miss);
+        if (b) {
+            L = base + __ffs(b) - 1;
+            break;
+        }
+    }
+    if (lane == 0) {
+        prog->verify_accept[0] = L;
+        prog->verify_accept[1] = argmax[L];
     }
 }
 
@@ -843,6 +874,14 @@ BI_API bi_status bi_program_build(const bi_op *ops, int n_ops, void *program, si
             if (!o.q || !o.s_a || !o.w_q || !o.s_w || o.N < 1 || o.M > 16) return BI_ERR_INVALID_ARG;
             if (o.kind == BI_OP_LINEAR && !o.y) return BI_ERR_INVALID_ARG;
             if (o.kind == BI_OP_LMHEAD && !o.argmax) return BI_ERR_INVALID_ARG;
+            if (o.accept && (o.kind != BI_OP_LMHEAD || (o.M > 1 && !o.draft))) return BI_ERR_INVALID_ARG;
+            if ((o.accept && !a4(o.accept)) || (o.draft && !a4(o.draft))) return BI_ERR_ALIGNMENT;
+            if (o.accept) {
+                h->verify_M = o.M;
+                h->verify_argmax = o.argmax;
+                h->verify_draft = o.draft;
+                h->verify_accept = o.accept;
+            }
             if (!a16(o.q) || !a16(o.w_q) || !a4(o.s_a) || !a4(o.s_w) || (o.argmax && !a4(o.argmax)))
                 return BI_ERR_ALIGNMENT;
             d.q = o.q;
@@ -881,8 +920,13 @@ BI_API bi_status bi_program_run(const void *program, int max_tokens, void *ws, s
         return BI_ERR_UNSUPPORTED;
     if (major != 10 || minor != 3) return BI_ERR_UNSUPPORTED;
     const int grid = 2 * sms < bi::kProgMaxGrid ? 2 * sms : bi::kProgMaxGrid;   // two CTAs per SM
-    const cudaError_t e = max_tokens > 8 ? bi::launch_program<2>(program, ws, grid, stream)
-                                         : bi::launch_program<1>(program, ws, grid, stream);
+    cudaError_t e = max_tokens > 8 ? bi::launch_program<2>(program, ws, grid, stream)
+                                   : bi::launch_program<1>(program, ws, grid, stream);
+    if (e == cudaSuccess) {
+        // the verification of the drafts, if the program asks for it
+        bi::program_verify_kernel<<<1, 32, 0, stream>>>(static_cast<const bi::ProgHeader *>(program));
+        e = cudaGetLastError();
+    }
     return e == cudaSuccess ? BI_OK : BI_ERR_CUDA;
 }
 

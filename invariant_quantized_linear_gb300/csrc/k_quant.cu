@@ -313,6 +313,26 @@ __global__ void __launch_bounds__(kQuantThreads) requant_pow2_kernel(const int8_
     if (threadIdx.x == 0) s_w_out[row] = s_new;
 }
 
+// L = first i < M - 1 with argmax[i] != draft[i] (M - 1 if none); out = {L, argmax[L]}.
+__global__ void greedy_verify_kernel(const int32_t *argmax, const int32_t *draft, int M, int32_t *out)
+{
+    const int lane = threadIdx.x;
+    int L = M - 1;
+    for (int base = 0; base < M - 1; base += 32) {
+        const int i = base + lane;
+        const bool miss = i < M - 1 && argmax[i] != draft[i];
+        const unsigned b = __ballot_sync(0xffffffffu, miss);
+        if (b) {
+            L = base + __ffs(b) - 1;
+            break;
+        }
+    }
+    if (lane == 0) {
+        out[0] = L;
+        out[1] = argmax[L];
+    }
+}
+
 // One thread waits, with the library's bounded wait, on a barrier phase that
 // nothing will complete; when the wait gives up it reports a timeout in the
 // status word, as the linear and program kernels do.
@@ -347,6 +367,13 @@ cudaError_t launch_relu_mul_quantize(const uint16_t *gu, int64_t ldgu, int M, in
 {
     const RowArgs a = {gu, ldgu, m_out, K, q, s_a};
     return launch_rows<kRowReluMul>(a, M, pdl, stream);
+}
+
+cudaError_t launch_greedy_verify(const int32_t *argmax, const int32_t *draft, int M, int32_t *out,
+                                 cudaStream_t stream)
+{
+    greedy_verify_kernel<<<1, 32, 0, stream>>>(argmax, draft, M, out);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_wait_selftest(int *status, cudaStream_t stream)

@@ -144,3 +144,12 @@ def test_program_build_validation(bi):
     assert one(kind=bi.BI_OP_RELU_MUL_QUANT, ldx=2048, y=FAKE + 2048) == bi.BI_ERR_INVALID_ARG  # m in gu
     assert one(kind=bi.BI_OP_QUANTIZE_ACT, y=FAKE + 8192) == bi.BI_ERR_INVALID_ARG  # plain kind has no y
     assert one(kind=9) == bi.BI_ERR_INVALID_ARG
+
+
+def test_greedy_verify_validation(bi):
+    V = bi.lib.bi_greedy_verify
+    assert V(None, FAKE, 4, FAKE, None) == bi.BI_ERR_INVALID_ARG
+    assert V(FAKE, None, 4, FAKE, None) == bi.BI_ERR_INVALID_ARG          # drafts needed for M > 1
+    assert V(FAKE, FAKE, 0, FAKE, None) == bi.BI_ERR_INVALID_ARG
+    assert V(FAKE + 2, FAKE, 4, FAKE, None) == bi.BI_ERR_ALIGNMENT
+    assert V(FAKE, FAKE, 4, FAKE + 1, None) == bi.BI_ERR_ALIGNMENT

@@ -77,3 +77,45 @@ def test_lmhead_full_size_with_near_ties(bi):
         am, lg = lmhead(bi, q[:M].contiguous(), s[:M].contiguous(), wq, sw, flags=bi.BI_FLAG_PDL)
         assert np.array_equal(to_np(am), am_o[:M]), M
         assert np.array_equal(to_np(lg), lg_o[:M]), M
+
+
+@pytest.mark.parametrize("M", [1, 2, 5, 16, 40, 100])
+def test_greedy_verify_matches_oracle(bi, M):
+    rng = np.random.default_rng(200 + M)
+    for trial in range(20):
+        am = rng.integers(0, 5, M).astype(np.int32)
+        dr = am[:M - 1].copy()
+        cut = int(rng.integers(0, M))
+        if cut < M - 1:
+            dr[cut] = dr[cut] + 1
+        out = torch.full((2,), -1, dtype=torch.int32, device=DEV)
+        bi.bi_greedy_verify(to_dev(am), to_dev(dr) if M > 1 else None, out)
+        assert tuple(to_np(out).tolist()) == oracle.greedy_verify(am, dr), (trial, cut)
+
+
+@pytest.mark.parametrize("M,cut", [(8, 3), (8, 7), (5, 0), (1, 0), (16, 11)])
+def test_program_head_greedy_verify(bi, M, cut):
+    """An LM-head op with drafted tokens reports the accepted count and the
+    next token, as the oracle computes them from the oracle's argmax."""
+    K, N = 1024, 3000
+    x = gen.act_bf16(300 + M, 1, M, K)
+    w = gen.weight_f32(300 + M, 0, 0, N, K)
+    q_o, s_o = oracle.quantize_act(x)
+    wq_o, sw_o = oracle_weights(oracle, w, True)
+    am_o, _ = oracle.lmhead_argmax(q_o, s_o, wq_o, sw_o, want_logits=False)
+    dr = am_o[:M - 1].copy()
+    if cut < M - 1:
+        dr[cut] = (dr[cut] + 1) % N
+    q, s = quant_act(bi, x)
+    wq, sw = weights(bi, w, True)
+    am = torch.full((M,), -1, dtype=torch.int32, device=DEV)
+    acc = torch.full((2,), -1, dtype=torch.int32, device=DEV)
+    dd = to_dev(dr) if M > 1 else None
+    ops = [bi.op_lmhead(q, s, wq, sw, None, am, draft=dd, accept=acc)]
+    prog = bi.new_program(1)
+    bi.bi_program_build(ops, prog)
+    ws = torch.zeros(bi.bi_program_workspace_size(), dtype=torch.uint8, device=DEV)
+    bi.bi_program_run(prog, M, ws)
+    torch.cuda.synchronize()
+    assert np.array_equal(to_np(am), am_o)
+    assert tuple(to_np(acc).tolist()) == oracle.greedy_verify(am_o, dr)
