@@ -65,6 +65,8 @@ def parse():
     p.add_argument("--layers", type=int, default=36)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-sweep", action="store_true", help="skip the per-M sweep")
+    p.add_argument("--prefill-only", type=int, default=0, metavar="M",
+                   help="time only the prefill contraction at M tokens and print its figures")
     p.add_argument("--mode", default="program", choices=["program", "calls"],
                    help="program: the step as one verify-pass program launch; calls: one launch per op")
     return p.parse_args()
@@ -307,7 +309,7 @@ class Stack:
         return sum(self.op_bytes(o) for o in self.ops(M) if o.kind == bi.BI_OP_LINEAR)
 
 
-def prefill_measure(bi, torch, st, stream, peaks):
+def prefill_measure(bi, torch, st, stream, peaks, Ms=(512, 2048)):
     """The prefill contraction (M = 512 and 2048 tokens, K = 4096, N = 12288:
     layer 0's gate projection) through bi_linear_w8a8, timed alone: int
     operations per second against the measured dense bf16 tensor peak (the
@@ -317,7 +319,7 @@ def prefill_measure(bi, torch, st, stream, peaks):
     K, N = 4096, 12288
     wq = st.W[0]["gu"][0][:N]
     sw = st.W[0]["gu"][1][:N]
-    for Mp in (512, 2048):
+    for Mp in Ms:
         x = torch.from_numpy(gen.activations(gen.PREFILL, Mp, K).view(np.int16)).to(st.dev)
         q = torch.empty((Mp, K), dtype=torch.int8, device=st.dev)
         s = torch.empty(Mp, dtype=torch.float32, device=st.dev)
@@ -339,8 +341,9 @@ def prefill_measure(bi, torch, st, stream, peaks):
         tops = 2.0 * Mp * N * K / (ms * 1e-3) / 1e12
         out[str(Mp)] = {"ms": round(ms, 4), "tops": round(tops, 1),
                         "frac_of_bf16_peak": round(tops / float(peaks["bf16_tflops"]), 4)}
-    out["note"] = ("y = W8A8(x) with K=4096, N=12288 (int8 x int8 -> exact int32 via f16 mma.sync); "
-                   "peak = measured cuBLAS dense bf16 (tcgen05), which sm_103a offers no int8 counterpart of")
+    out["note"] = ("y = W8A8(x) with K=4096, N=12288 (int8 x int8 -> exact int32: int8 converted to f16 in "
+                   "shared memory, tcgen05.mma kind::f16 into fp32 TMEM chunks of 1024 K, int32 totals); "
+                   "peak = measured cuBLAS dense bf16, since sm_103a's tcgen05 has no int8 kind")
     return out
 
 
@@ -371,6 +374,12 @@ def run_ours(args):
     setup_s = time.time() - t0
     flags = bi.BI_FLAG_PDL
     stream = torch.cuda.Stream(device=dev)
+    if args.prefill_only:
+        peaks, _ = read_peaks()
+        if rank == 0:
+            print(json.dumps({"prefill": prefill_measure(bi, torch, st, stream, peaks, Ms=(args.prefill_only,))}),
+                  flush=True)
+        return
 
     def barrier():
         torch.cuda.synchronize()

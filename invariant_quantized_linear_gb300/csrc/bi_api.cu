@@ -264,10 +264,8 @@ bi_status bi_linear_w8a8(const int8_t *q, const float *s_a, int M, int K, const 
     st = device_info(nullptr);
     if (st != BI_OK) return st;
     bi::PrefillArgs a;
-    st = encode_int8_2d(&a.map_w, w_q, N, K, 128, 128, false);
-    if (st != BI_OK) return st;
-    st = encode_int8_2d(&a.map_q, q, M, K, 128, 128, false);
-    if (st != BI_OK) return st;
+    a.q = q;
+    a.w_q = w_q;
     a.s_a = s_a;
     a.s_w = s_w;
     a.y = y;

@@ -1,17 +1,32 @@
-// Tiled W8A8 kernel for prefill-sized batches (M > 16): a dense int8
-// contraction with exact int32 accumulation and the same per-element
-// epilogue as the weight-streaming kernel, so every row matches it bitwise.
+// Tiled W8A8 kernel for prefill-sized batches (M > 16) on the tcgen05 tensor
+// cores: a dense int8 contraction with exact int32 results and the same
+// per-element epilogue as the weight-streaming kernel, so every row matches
+// it bitwise.
 //
-// sm_103a has no int8 kind for tcgen05.mma, and its warp-level int8 MMA runs
-// at a fraction of the f16 rate, so the contraction runs on f16 tensor-core
-// MMAs (m16n8k16, fp32 accumulate) over int8 values converted exactly to f16;
-// fp32 partials are moved into int32 totals while they are integers far below
-// 2^24, so the sum is the exact integer dot product.  Tiles are moved by TMA
-// into a ring of 128-byte-swizzled shared-memory stages by one producer warp;
-// eight consumer warps each own a 32-token x 64-row tile.
-// CTA tile: 128 tokens x 128 weight rows, 128 bytes of K per stage.
+// sm_103a's tcgen05.mma has no int8 kind, so the int8 codes are converted
+// exactly to f16 and multiplied by kind::f16 MMAs into fp32 accumulators in
+// tensor memory (TMEM).  Every product is an integer of magnitude <= 128^2,
+// so an fp32 sum of at most 1024 of them (<= 2^24) is exact; the fp32 sum of
+// each 1024-wide K chunk is moved into an int32 total, kept in the other half
+// of TMEM, before the next chunk starts.
+//
+// CTA tile: 128 tokens (MMA M = TMEM lanes) x 256 weight rows (MMA N = TMEM
+// columns), 64 K per stage.  Roles:
+//   warps 0-7   load the tile's int8 rows from global memory four stages
+//               ahead (into registers), convert them to f16 and store them
+//               into a ring of K-major, 128-byte-swizzled stages;
+//   warps 8-11  TMEM lane quarters 0-3: move chunk sums into the int32
+//               totals, then the epilogue, one token row per thread; warp 8
+//               also allocates TMEM, and its lane 0 issues the MMAs and
+//               commits them (the MMAs of a chunk wait for the previous
+//               chunk's move in any case).
+// Loading through registers rather than TMA keeps the int8 bytes out of
+// shared memory, whose bandwidth the MMA operands and the f16 stores share.
+// Every wait is bounded: on a timeout the kernel writes DEV_TIMEOUT to the
+// workspace status word and every role returns.
 #include "kernels.cuh"
 #include "ptx.cuh"
+#include "tc.cuh"
 
 #include <cuda_bf16.h>
 
@@ -19,192 +34,280 @@ namespace bi {
 
 namespace {
 
-constexpr int kWarpsM = 4, kWarpsN = 2;
-constexpr int kConsumers = kWarpsM * kWarpsN;
-constexpr int kThreads = (kConsumers + 1) * 32;
-constexpr int kTileM = 128, kTileN = 128, kTileK = 128;
-constexpr int kStageQ = kTileM * kTileK;   // 16 KB
-constexpr int kStageW = kTileN * kTileK;   // 16 KB
+constexpr int kTileM = 128;                       // tokens per tile: MMA M, TMEM lanes
+constexpr int kTileN = 256;                       // weight rows per tile: MMA N, TMEM columns
+constexpr int kStepK = 64;                        // K per stage: one 128-byte f16 row
 constexpr int kStages = 4;
-constexpr int kSmemBytes = kStages * (kStageQ + kStageW) + 1024 + 256;
+constexpr int kChunkSteps = 16;                   // 1024 K per exact fp32 chunk
+constexpr int kAhead = 4;                         // converter loads run this many steps ahead
+constexpr int kConvWarps = 8;
+constexpr int kConvThreads = kConvWarps * 32;
+constexpr int kEpiWarp0 = kConvWarps;             // warps 8 .. 11 (warp % 4 = lane quarter)
+constexpr int kThreads = (kEpiWarp0 + 4) * 32;    // 384: three warps per scheduler
+constexpr int kStageA = kTileM * 128;             // 16 KB of f16 tokens
+constexpr int kStageB = kTileN * 128;             // 32 KB of f16 weights
+constexpr int kStageBytes = kStageA + kStageB;
+constexpr uint32_t kTmemCols = 512;               // [0, 256) fp32 chunk sums, [256, 512) int32 totals
+constexpr uint32_t kTotCol = 256;
+constexpr int kChunksA = kTileM * 4 / kConvThreads;   // 16-byte int8 chunks per thread and stage: 2
+constexpr int kChunksB = kTileN * 4 / kConvThreads;   // 4
+constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kTileN * 4 + 256;
+
+static_assert(kTileM * 4 % kConvThreads == 0 && kTileN * 4 % kConvThreads == 0, "converter split");
+static_assert(kChunkSteps * kStepK * 128 * 128 <= (1 << 24), "chunk sums must stay exact in fp32");
 
 struct Params {
+    const int8_t *q;     // [M, K]
+    const int8_t *w;     // [N, K]
     const float *s_a;
     const float *s_w;
-    uint16_t *y;
+    uint16_t *y;         // [M, N] bf16
     int M, N, K;
-    int kt;  // K tiles
+    int kt;              // K steps
+    int vec_y;           // y rows allow 16-byte stores
     Workspace ws;
     int pdl;
 };
 
-__global__ void __launch_bounds__(kThreads, 1)
-    prefill_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_q, Params p)
+// 16 int8 values -> 16 f16 values, stored as two 16-byte chunks (2c, 2c + 1)
+// of a 128-byte swizzled row.
+__device__ __forceinline__ void store_f16_row(uint8_t *row_base, int row, int c, uint4 v)
+{
+    uint32_t h[8];
+    i8x4_to_f16x2x2(v.x, h[0], h[1]);
+    i8x4_to_f16x2x2(v.y, h[2], h[3]);
+    i8x4_to_f16x2x2(v.z, h[4], h[5]);
+    i8x4_to_f16x2x2(v.w, h[6], h[7]);
+    const int sw = row & 7;
+    *reinterpret_cast<uint4 *>(row_base + (((2 * c) ^ sw) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<uint4 *>(row_base + (((2 * c + 1) ^ sw) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
+}
+
+__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(Params p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *sQ = smem;                                  // [stages][128 tokens][128 B]
-    uint8_t *sW = smem + kStages * kStageQ;              // [stages][128 rows][128 B]
-    uint64_t *full = reinterpret_cast<uint64_t *>(sW + kStages * kStageW);
-    uint64_t *empty = full + kStages;
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + kStages);
+    float *sw_tile = reinterpret_cast<float *>(smem + kStages * kStageBytes);     // [kTileN]
+    uint64_t *full = reinterpret_cast<uint64_t *>(sw_tile + kTileN);             // converters -> MMA
+    uint64_t *empty = full + kStages;                                             // MMA done reading
+    uint64_t *acc_full = empty + kStages;                                         // chunk sum ready
+    uint64_t *acc_empty = acc_full + 1;                                           // chunk sum moved
+    uint64_t *drain = acc_empty + 1;                                              // all MMAs complete
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n0 = blockIdx.x * kTileN;
-    const int m0 = blockIdx.y * kTileM;
+    const int m0 = blockIdx.x * kTileM;
+    const int n0 = blockIdx.y * kTileN;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kConsumers);
+            mbar_init(&full[s], kConvWarps);       // one arrival per converter warp
+            mbar_init(&empty[s], 1);               // MMA commit
         }
+        mbar_init(acc_full, 1);                    // MMA commit
+        mbar_init(acc_empty, 4);                   // the four epilogue warps
+        mbar_init(drain, 1);
         *abort_flag = 0;
         fence_mbarrier_init();
     }
+    if (warp == kEpiWarp0) tc::tmem_alloc(tmem_slot, kTmemCols);
+    tc::fence_before();
     __syncthreads();
+    tc::fence_after();
+    const uint32_t tmem = *tmem_slot;
     if (p.pdl) pdl_launch_dependents();
 
-    if (warp == kConsumers) {
-        if (lane == 0) {
-            prefetch_tensormap(&map_w);
-            prefetch_tensormap(&map_q);
-            const uint64_t pol = policy_evict_last();  // both operands are re-read by other CTAs
-            if (p.pdl) pdl_wait();
-            int issued = 0;
-            for (int j = 0; j < p.kt; ++j) {
-                const int s = j % kStages;
-                if (j >= kStages && !mbar_wait_bounded(&empty[s], ((j / kStages) - 1) & 1, abort_flag)) {
-                    *abort_flag = 1;
-                    atomicExch(p.ws.status, DEV_TIMEOUT);
+    auto fail = [&]() {
+        if (!*abort_flag) {
+            *abort_flag = 1;
+            atomicExch(p.ws.status, DEV_TIMEOUT);
+        }
+    };
+
+    if (warp < kConvWarps) {
+        // ------------------------------------------------ int8 -> f16 stages
+        const int t = threadIdx.x;
+        const int c = t & 3;        // 16-byte chunk of the 64-byte int8 row slice
+        const int r0 = t >> 2;      // rows r0 + 64 i
+        if (p.pdl) pdl_wait();
+        auto load = [&](int j, uint4 (&ra)[kChunksA], uint4 (&rb)[kChunksB]) {
+            const int k = j * kStepK + 16 * c;
+            const bool kin = k < p.K;
+#pragma unroll
+            for (int i = 0; i < kChunksA; ++i) {
+                const int tok = m0 + r0 + 64 * i;
+                ra[i] = (kin && tok < p.M)
+                            ? __ldg(reinterpret_cast<const uint4 *>(p.q + static_cast<size_t>(tok) * p.K + k))
+                            : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int i = 0; i < kChunksB; ++i) {
+                const int n = n0 + r0 + 64 * i;
+                rb[i] = (kin && n < p.N)
+                            ? __ldg(reinterpret_cast<const uint4 *>(p.w + static_cast<size_t>(n) * p.K + k))
+                            : make_uint4(0, 0, 0, 0);
+            }
+        };
+        auto step = [&](int j, uint4 (&ra)[kChunksA], uint4 (&rb)[kChunksB]) -> bool {
+            const int s = j % kStages;
+            if (j >= kStages && !mbar_wait_bounded(&empty[s], ((j / kStages) - 1) & 1, abort_flag)) {
+                fail();
+                return false;
+            }
+            uint8_t *sa = smem + s * kStageBytes;
+            uint8_t *sb = sa + kStageA;
+#pragma unroll
+            for (int i = 0; i < kChunksA; ++i) store_f16_row(sa + (r0 + 64 * i) * 128, r0 + 64 * i, c, ra[i]);
+#pragma unroll
+            for (int i = 0; i < kChunksB; ++i) store_f16_row(sb + (r0 + 64 * i) * 128, r0 + 64 * i, c, rb[i]);
+            fence_proxy_async_smem();   // the tensor core reads the stage through the async proxy
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&full[s]);
+            if (j + kAhead < p.kt) load(j + kAhead, ra, rb);
+            return true;
+        };
+        // kAhead register sets: the loads of step j + kAhead are issued when
+        // step j is stored, which covers the L2 latency under load
+        uint4 ra0[kChunksA], rb0[kChunksB], ra1[kChunksA], rb1[kChunksB];
+        uint4 ra2[kChunksA], rb2[kChunksB], ra3[kChunksA], rb3[kChunksB];
+        load(0, ra0, rb0);
+        if (p.kt > 1) load(1, ra1, rb1);
+        if (p.kt > 2) load(2, ra2, rb2);
+        if (p.kt > 3) load(3, ra3, rb3);
+        for (int j = 0; j < p.kt; j += kAhead) {
+            if (!step(j, ra0, rb0)) break;
+            if (j + 1 < p.kt && !step(j + 1, ra1, rb1)) break;
+            if (j + 2 < p.kt && !step(j + 2, ra2, rb2)) break;
+            if (j + 3 < p.kt && !step(j + 3, ra3, rb3)) break;
+        }
+    } else {
+        // ------------------------------------------------ MMA issue, chunk moves, epilogue
+        // warp 8 + qd reads TMEM lanes 32 qd .. 32 qd + 31 (token rows of
+        // the tile); warp 8 also issues each chunk's MMAs (lane 0)
+        const int qd = warp - kEpiWarp0;
+        const int et = threadIdx.x - kEpiWarp0 * 32;
+        const bool issuer = (qd == 0);
+        if (p.pdl) pdl_wait();
+        for (int i = et; i < kTileN; i += 128) sw_tile[i] = (n0 + i < p.N) ? p.s_w[n0 + i] : 0.0f;
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        const int tok = m0 + 32 * qd + lane;
+        const float sa = tok < p.M ? p.s_a[tok] : 0.0f;
+        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * qd) << 16);
+        const int nch = (p.kt + kChunkSteps - 1) / kChunkSteps;
+        constexpr uint32_t idesc = tc::idesc_f16_f32(kTileM, kTileN);
+        int j = 0;
+        for (int ch = 0; ch < nch; ++ch) {
+            if (issuer) {
+                bool ok = true;
+                if (ch > 0) {
+                    // the previous chunk's sum must have left D (all four warps)
+                    ok = __all_sync(0xffffffffu, mbar_wait_bounded(acc_empty, (ch - 1) & 1, abort_flag));
+                    tc::fence_after();
+                }
+                const int jend = min(p.kt, (ch + 1) * kChunkSteps);
+                for (; ok && j < jend; ++j) {
+                    const int s = j % kStages;
+                    ok = __all_sync(0xffffffffu, mbar_wait_bounded(&full[s], (j / kStages) & 1, abort_flag));
+                    if (!ok) break;
+                    tc::fence_after();
+                    if (lane == 0) {
+                        const uint32_t a0 = smem_u32(smem + s * kStageBytes);
+                        const uint32_t b0 = a0 + kStageA;
+                        const int kc = j % kChunkSteps;
+#pragma unroll
+                        for (int k = 0; k < kStepK / 16; ++k)
+                            tc::mma_f16_ss(tmem, tc::sdesc_kmajor_sw128(a0 + 32 * k),
+                                           tc::sdesc_kmajor_sw128(b0 + 32 * k), idesc, (kc | k) != 0 ? 1u : 0u);
+                        tc::commit(&empty[s]);
+                        if (j == jend - 1) tc::commit(acc_full);
+                    }
+                    __syncwarp();
+                }
+                if (!ok) {
+                    fail();
                     break;
                 }
-                mbar_arrive_expect_tx(&full[s], kStageQ + kStageW);
-                tma_load_2d(sQ + s * kStageQ, &map_q, &full[s], j * kTileK, m0, pol);
-                tma_load_2d(sW + s * kStageW, &map_w, &full[s], j * kTileK, n0, pol);
-                issued = j + 1;
             }
-            if (*abort_flag) {
-                volatile int never = 0;
-                const int first = issued > kStages ? issued - kStages : 0;
-                for (int j = first; j < issued; ++j) mbar_wait_bounded(&full[j % kStages], (j / kStages) & 1, &never);
+            // warp-uniform: the TMEM loads below are warp-collective
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(acc_full, ch & 1, abort_flag))) {
+                fail();
+                break;
             }
-        }
-        return;
-    }
-
-    if (p.pdl) pdl_wait();
-    const int wm = warp % kWarpsM, wn = warp / kWarpsM;   // warp tile: tokens wm*32.., rows wn*64..
-    const int g = lane >> 2, tq = lane & 3;
-    const int mat = lane >> 3, r8 = lane & 7;
-    // A operand (tokens): x4 = (tok 0-7, X), (tok 8-15, X), (tok 0-7, Y), (tok 8-15, Y)
-    const uint32_t a_tok = wm * 32 + ((mat & 1) ? 8 : 0) + r8;
-    const int a_hi = (mat >> 1) & 1;
-    // B operand (weight rows): x4 = (rows 0-7, X), (rows 0-7, Y), (rows 8-15, X), (rows 8-15, Y)
-    const uint32_t b_row = wn * 64 + ((mat & 2) ? 8 : 0) + r8;
-    const int b_hi = mat & 1;
-
-    // int32 totals; fp32 tensor-core partials are moved into them every two
-    // stages (256 bytes of K: |partial| <= 256 * 127^2 < 2^22, exact in fp32)
-    int32_t acc[2][8][4];
-    float facc[2][8][4];
+            tc::fence_after();
+            if (ch + 1 < nch) {
+#pragma unroll 1
+                for (int col = 0; col < kTileN; col += 32) {
+                    uint32_t d[32], tot[32];
+                    tc::ld32(lane_addr + col, d);
+                    if (ch > 0) tc::ld32(lane_addr + kTotCol + col, tot);
+                    tc::wait_ld();
 #pragma unroll
-    for (int i = 0; i < 2; ++i)
-#pragma unroll
-        for (int jn = 0; jn < 8; ++jn)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                acc[i][jn][e] = 0;
-                facc[i][jn][e] = 0.0f;
-            }
-
-    for (int j = 0; j < p.kt; ++j) {
-        const int s = j % kStages;
-        if (*abort_flag || !mbar_wait_bounded(&full[s], (j / kStages) & 1, abort_flag)) {
-            if (!*abort_flag) {
-                *abort_flag = 1;
-                atomicExch(p.ws.status, DEV_TIMEOUT);
-            }
-            break;
-        }
-        const uint32_t qb = smem_u32(sQ + s * kStageQ);
-        const uint32_t wb = smem_u32(sW + s * kStageW);
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-            // int8 fragments of 32 bytes of K (chunks X and Y)
-            uint32_t a8[2][4];
-#pragma unroll
-            for (int i = 0; i < 2; ++i)
-                ldmatrix_x4(qb + swz128(a_tok + 16 * i, 2 * ks + a_hi), a8[i][0], a8[i][1], a8[i][2], a8[i][3]);
-            uint32_t b8[4][4];
-#pragma unroll
-            for (int jp = 0; jp < 4; ++jp)
-                ldmatrix_x4(wb + swz128(b_row + 16 * jp, 2 * ks + b_hi), b8[jp][0], b8[jp][1], b8[jp][2], b8[jp][3]);
-#pragma unroll
-            for (int xy = 0; xy < 2; ++xy) {
-                uint32_t a[2][4];
-#pragma unroll
-                for (int i = 0; i < 2; ++i) {
-                    i8x4_to_f16x2x2(a8[i][2 * xy], a[i][0], a[i][2]);      // token g
-                    i8x4_to_f16x2x2(a8[i][2 * xy + 1], a[i][1], a[i][3]);  // token g + 8
+                    for (int e = 0; e < 32; ++e) {
+                        const int32_t v = f2i_exact(__uint_as_float(d[e]));
+                        tot[e] = ch > 0 ? static_cast<uint32_t>(static_cast<int32_t>(tot[e]) + v) : static_cast<uint32_t>(v);
+                    }
+                    tc::st32(lane_addr + kTotCol + col, tot);
                 }
+                tc::wait_st();
+                tc::fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(acc_empty);
+            } else {
+                uint16_t *yr = p.y + static_cast<size_t>(tok < p.M ? tok : 0) * p.N;
+#pragma unroll 1
+                for (int col = 0; col < kTileN; col += 32) {
+                    uint32_t d[32], tot[32];
+                    __syncwarp();   // reconverge after the ragged stores of the previous columns
+                    tc::ld32(lane_addr + col, d);
+                    if (ch > 0) tc::ld32(lane_addr + kTotCol + col, tot);
+                    tc::wait_ld();
+                    if (tok >= p.M) continue;
+                    uint32_t o[16];
 #pragma unroll
-                for (int jp = 0; jp < 4; ++jp) {
-                    uint32_t b0, b1, b2, b3;
-                    i8x4_to_f16x2x2(b8[jp][xy], b0, b1);       // rows 0-7 of the pair
-                    i8x4_to_f16x2x2(b8[jp][2 + xy], b2, b3);   // rows 8-15
+                    for (int e = 0; e < 32; e += 2) {
+                        uint32_t b2 = 0;
 #pragma unroll
-                    for (int i = 0; i < 2; ++i) {
-                        mma_f16_16816(facc[i][2 * jp], a[i][0], a[i][1], a[i][2], a[i][3], b0, b1);
-                        mma_f16_16816(facc[i][2 * jp + 1], a[i][0], a[i][1], a[i][2], a[i][3], b2, b3);
+                        for (int h = 0; h < 2; ++h) {
+                            int32_t acc = f2i_exact(__uint_as_float(d[e + h]));
+                            if (ch > 0) acc += static_cast<int32_t>(tot[e + h]);
+                            float f = __int2float_rn(acc);
+                            f = __fmul_rn(f, sa);
+                            f = __fmul_rn(f, sw_tile[col + e + h]);
+                            b2 |= static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(f))) << (16 * h);
+                        }
+                        o[e >> 1] = b2;
+                    }
+                    const int n = n0 + col;
+                    if (p.vec_y && n + 32 <= p.N) {
+#pragma unroll
+                        for (int v = 0; v < 4; ++v)
+                            *reinterpret_cast<uint4 *>(yr + n + 8 * v) =
+                                make_uint4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            if (n + e < p.N) yr[n + e] = static_cast<uint16_t>(o[e >> 1] >> (16 * (e & 1)));
                     }
                 }
             }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
-        if ((j & 1) || j + 1 == p.kt) {
-#pragma unroll
-            for (int i = 0; i < 2; ++i)
-#pragma unroll
-                for (int jn = 0; jn < 8; ++jn)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        acc[i][jn][e] += f2i_exact(facc[i][jn][e]);
-                        facc[i][jn][e] = 0.0f;
-                    }
+        tc::fence_before();
+        if (issuer) {
+            // nothing may still read shared memory or write TMEM when the CTA
+            // frees them
+            if (lane == 0) tc::commit(drain);
+            volatile int never = 0;
+            mbar_wait_bounded(drain, 0, &never);
         }
     }
-    if (*abort_flag) return;
-
-    // epilogue: acc[i][jn] = (token wm*32 + 16i + g (+8), row wn*64 + 8jn + 2tq (+1))
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int tok = m0 + wm * 32 + 16 * i + g + 8 * h;
-            if (tok >= p.M) continue;
-            const float sa = p.s_a[tok];
-            uint16_t *yr = p.y + static_cast<size_t>(tok) * p.N;
-#pragma unroll
-            for (int jn = 0; jn < 8; ++jn) {
-                const int n = n0 + wn * 64 + 8 * jn + 2 * tq;
-                uint16_t b[2];
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int nn = n + e;
-                    float f = __int2float_rn(acc[i][jn][2 * h + e]);
-                    f = __fmul_rn(f, sa);
-                    f = __fmul_rn(f, nn < p.N ? p.s_w[nn] : 0.0f);
-                    b[e] = __bfloat16_as_ushort(__float2bfloat16_rn(f));
-                }
-                if (n + 1 < p.N && ((reinterpret_cast<uintptr_t>(yr + n) & 3u) == 0)) {
-                    *reinterpret_cast<uint32_t *>(yr + n) = static_cast<uint32_t>(b[0]) | (static_cast<uint32_t>(b[1]) << 16);
-                } else {
-                    if (n < p.N) yr[n] = b[0];
-                    if (n + 1 < p.N) yr[n + 1] = b[1];
-                }
-            }
-        }
+    __syncwarp();
+    tc::fence_before();
+    __syncthreads();
+    if (warp == kEpiWarp0) {
+        tc::fence_after();
+        tc::tmem_dealloc(tmem, kTmemCols);
     }
 }
 
@@ -219,17 +322,21 @@ cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream)
         attr_set = true;
     }
     Params p;
+    p.q = a.q;
+    p.w = a.w_q;
     p.s_a = a.s_a;
     p.s_w = a.s_w;
     p.y = a.y;
     p.M = a.M;
     p.N = a.N;
     p.K = a.K;
-    p.kt = (a.K + kTileK - 1) / kTileK;
+    p.kt = (a.K + kStepK - 1) / kStepK;
+    p.vec_y = ((a.N % 8) == 0 && (reinterpret_cast<uintptr_t>(a.y) & 15u) == 0) ? 1 : 0;
     p.ws = a.ws;
     p.pdl = a.pdl ? 1 : 0;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>((a.N + kTileN - 1) / kTileN), static_cast<unsigned>((a.M + kTileM - 1) / kTileM));
+    // token tiles fastest: the CTAs resident together share weight tiles in L2
+    cfg.gridDim = dim3(static_cast<unsigned>((a.M + kTileM - 1) / kTileM), static_cast<unsigned>((a.N + kTileN - 1) / kTileN));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = stream;
@@ -238,7 +345,7 @@ cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = a.pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, prefill_kernel, a.map_w, a.map_q, p);
+    return cudaLaunchKernelEx(&cfg, prefill_kernel, p);
 }
 
 }  // namespace bi

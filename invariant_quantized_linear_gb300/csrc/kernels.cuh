@@ -9,7 +9,8 @@ namespace bi {
 
 // ---------------------------------------------------------------- workspace
 //
-// One layout serves the skinny linear, the LM head and the prefill kernel:
+// One layout serves the skinny linear, the LM head and the prefill kernel
+// (which uses only the status word):
 //   [0, 256)          control words: status (int), argmax ticket (int)
 //   rb_counter        kMaxGrid int32   split-K chunk counters, one per slot
 //   best              kMaxGrid * 16 uint64   per-CTA argmax keys
@@ -79,8 +80,8 @@ struct SkinnyArgs {
 cudaError_t launch_skinny(const SkinnyArgs &a, cudaStream_t stream);
 
 struct PrefillArgs {
-    CUtensorMap map_w;         // W [N, K], box 128 B x 128 rows, 128B swizzle
-    CUtensorMap map_q;         // q [M, K], box 128 B x 128 rows, 128B swizzle
+    const int8_t *q;           // [M, K], rows 16-byte aligned
+    const int8_t *w_q;         // [N, K], rows 16-byte aligned
     const float *s_a;
     const float *s_w;
     uint16_t *y;
@@ -89,7 +90,7 @@ struct PrefillArgs {
     bool pdl;
 };
 
-// M > 16 tiled kernel.
+// M > 16 tiled kernel (tcgen05).
 cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream);
 
 }  // namespace bi

@@ -41,7 +41,10 @@ def _check_linear(bi, x, w, pow2, flags=0):
 # the prefill kernel (M > 16)
 SKINNY = [(1, 1, 16), (2, 17, 48), (3, 100, 272), (8, 1000, 1024), (9, 1024, 1040), (16, 333, 4096),
           (4, 4096, 4096), (5, 64, 12288), (1, 12288, 256)]
-PREFILL = [(17, 130, 256), (33, 257, 1024), (130, 300, 528), (200, 1000, 4096), (64, 64, 16)]
+PREFILL = [(17, 130, 256), (33, 257, 1024), (130, 300, 528), (200, 1000, 4096), (64, 64, 16),
+           # exact fp32 chunks of 1024 K: a one-step last chunk, N tails on and
+           # off the 16-byte store path, several token and weight tiles
+           (129, 520, 1040), (300, 776, 3088)]
 
 
 @pytest.mark.parametrize("M,N,K", SKINNY + PREFILL)
