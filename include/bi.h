@@ -234,6 +234,23 @@ BI_API bi_status bi_greedy_verify(const int32_t *argmax, const int32_t *draft, i
 BI_API bi_status bi_selftest_wait_timeout(void *ws, size_t ws_bytes, bi_stream_t stream);
 
 /*
+ * Exhaustive check of the quotient the verify-pass executor quantises with.
+ * Codes are clamp(rne(v / s), -127, 127) with v / s an IEEE fp32 division
+ * (the per-token absmax quantisation of the W8A8 page, "Quantization").  The
+ * executor forms v / s from r = RN(1/s) by one fused-multiply-add correction
+ * instead of dividing.  This runs, for every positive finite bf16 row maximum
+ * amax (scale s = RN(amax / 127) >= 2^-64) and every bf16 v with |v| <= amax
+ * (about 0.99e9 pairs), that quotient and the IEEE division, and counts the
+ * pairs whose codes differ or whose quotients differ at |v / s| >= 2^-8
+ * (smaller quotients have code 0 either way).
+ *   out  device, 8-byte aligned, 3 x uint64, overwritten: [0] pairs checked,
+ *        [1] mismatches, [2] one mismatching pair (amax bits << 16 | v bits)
+ *        or 0.  Read it after the stream completes.
+ * Returns BI_ERR_INVALID_ARG for a null or misaligned `out`.
+ */
+BI_API bi_status bi_selftest_quotient(unsigned long long *out, bi_stream_t stream);
+
+/*
  * Verify-pass executor: a program of ops run by one persistent kernel.
  *
  * A decode or verify pass is a chain of small dependent steps (quantise an

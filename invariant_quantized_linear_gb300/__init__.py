@@ -50,6 +50,8 @@ lib.bi_greedy_verify.argtypes = [_vp, _vp, _ci, _vp, _vp]
 lib.bi_greedy_verify.restype = _ci
 lib.bi_selftest_wait_timeout.argtypes = [_vp, _sz, _vp]
 lib.bi_selftest_wait_timeout.restype = _ci
+lib.bi_selftest_quotient.argtypes = [_vp, _vp]
+lib.bi_selftest_quotient.restype = _ci
 lib.bi_workspace_status.argtypes = [_vp, _sz, _vp]
 lib.bi_workspace_status.restype = _ci
 lib.bi_linear_w8a8_noalloc.argtypes = [_vp, _vp, _ci, _ci, _vp, _vp, _ci, _vp, _cu, _vp]
@@ -270,6 +272,13 @@ def bi_selftest_wait_timeout(ws: torch.Tensor, stream=None) -> None:
     status then reads BI_ERR_TIMEOUT."""
     _check(lib.bi_selftest_wait_timeout(_ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
            "bi_selftest_wait_timeout")
+
+
+def bi_selftest_quotient(out: torch.Tensor, stream=None) -> None:
+    """out int64 [3] on the device: pairs checked, mismatches, one mismatching
+    (amax bits << 16 | v bits) of the executor's quotient against IEEE division."""
+    assert out.dtype == torch.int64 and out.numel() >= 3 and out.is_cuda
+    _check(lib.bi_selftest_quotient(_ptr(out), _stream(stream)), "bi_selftest_quotient")
 
 
 def bi_workspace_status(ws: torch.Tensor, stream=None) -> int:

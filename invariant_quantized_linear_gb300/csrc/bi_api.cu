@@ -305,6 +305,14 @@ bi_status bi_selftest_wait_timeout(void *ws, size_t ws_bytes, bi_stream_t stream
     return from_cuda(bi::launch_wait_selftest(static_cast<int *>(ws), stream));
 }
 
+bi_status bi_selftest_quotient(unsigned long long *out, bi_stream_t stream)
+{
+    if (!out || (reinterpret_cast<uintptr_t>(out) & 7u) != 0) return BI_ERR_INVALID_ARG;
+    const bi_status st = device_info(nullptr);
+    if (st != BI_OK) return st;
+    return from_cuda(bi::launch_quotient_selftest(out, stream));
+}
+
 bi_status bi_workspace_status(void *ws, size_t ws_bytes, bi_stream_t stream)
 {
     if (!ws || ws_bytes < bi::kWsBytes) return BI_ERR_WORKSPACE;

@@ -407,32 +407,27 @@ __global__ void __launch_bounds__(kThreads, 2) program_kernel(const ProgHeader *
                 const float s = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 127.0f);
                 const float r = __frcp_rn(s);
                 // each thread writes only chunks it read itself (in-place h is safe)
-                auto emit = [&](uint4 t, int ci) {
+                auto emit = [&](uint4 t, int ci, bool fast) {
                     if (kind == BI_OP_RESIDUAL_QUANT) {
                         t = rescale8(t, p2);
                         *reinterpret_cast<uint4 *>(hr + ci * 8) = t;
                     } else if (kind == BI_OP_RELU_MUL_QUANT && hr) {
                         *reinterpret_cast<uint4 *>(hr + ci * 8) = t;
                     }
-                    const uint32_t w4[4] = {t.x, t.y, t.z, t.w};
-                    uint32_t o[2] = {0, 0};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int lo = quant_code(bf16_lo(w4[e]), s, r);
-                        const int hi = quant_code(bf16_hi(w4[e]), s, r);
-                        o[e >> 1] |= ((static_cast<uint32_t>(lo) & 0xFFu) | ((static_cast<uint32_t>(hi) & 0xFFu) << 8))
-                                     << (16 * (e & 1));
-                    }
-                    *reinterpret_cast<uint2 *>(op.q + static_cast<long long>(m) * op.K + ci * 8) = make_uint2(o[0], o[1]);
+                    *reinterpret_cast<uint2 *>(op.q + static_cast<long long>(m) * op.K + ci * 8) =
+                        fast ? quant8(t, s, r) : quant8_div(t, s);
                 };
-                if (in_regs) {
+                if (in_regs && s >= kQuotientMinScale) {
 #pragma unroll
                     for (int c = 0; c < kRegChunks; ++c) {
                         const int ci = c * kT + ctid;
-                        if (ci < nchunk) emit(v[c], ci);
+                        if (ci < nchunk) emit(v[c], ci, true);
                     }
                 } else {
-                    for (int ci = ctid; ci < nchunk; ci += kT) emit(load_in(ci), ci);
+                    // rows too long for registers, or with a tiny scale
+                    const bool fast = s >= kQuotientMinScale;
+#pragma unroll 1
+                    for (int ci = ctid; ci < nchunk; ci += kT) emit(load_in(ci), ci, fast);
                 }
                 if (ctid == 0) op.s_a[m] = s;
                 fence_proxy_async_global();   // the codes are read by other CTAs' TMA

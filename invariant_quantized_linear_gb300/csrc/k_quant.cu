@@ -346,7 +346,55 @@ __global__ void wait_selftest_kernel(int *status)
     if (!mbar_wait_bounded(&bar, 0, &never)) atomicExch(status, DEV_TIMEOUT);
 }
 
+// Every (v, amax) a quantisation row can meet: amax a positive finite bf16
+// value, v a bf16 value with |v| <= amax.  For every row scale s =
+// RN(amax / 127) >= kQuotientMinScale, quotient_rn(v, s, RN(1/s)) is compared
+// with IEEE division: the code always, the value wherever IEEE division's
+// quotient is at least 2^-8.  One block per amax bit pattern.
+// out[0] += pairs checked, out[1] += mismatches, out[2] = a mismatch found
+// (amax bits << 16 | v bits), if any.
+__global__ void __launch_bounds__(256) quotient_selftest_kernel(unsigned long long *out)
+{
+    const uint32_t a_bits = blockIdx.x + 1u;   // 0x0001 .. 0x7F7F
+    const float amax = __uint_as_float(a_bits << 16);
+    const float s = __fdiv_rn(amax, 127.0f);
+    if (s < kQuotientMinScale) return;
+    const float r = __frcp_rn(s);
+    unsigned long long checked = 0, bad = 0;
+    for (uint32_t vb = threadIdx.x; vb <= a_bits; vb += blockDim.x)
+        for (uint32_t sign = 0; sign < 2; ++sign) {
+            const uint32_t v_bits = vb | (sign << 15);
+            const float v = __uint_as_float(v_bits << 16);
+            const float q = quotient_rn(v, s, r);
+            const float q_ref = __fdiv_rn(v, s);
+            ++checked;
+            // codes always; quotients from 2^-8 up, where every code is
+            // decided (smaller quotients round to code 0 either way)
+            if (code_byte(q) != code_byte(q_ref) || (fabsf(q_ref) >= 0x1p-8f && q != q_ref)) {
+                ++bad;
+                out[2] = (static_cast<unsigned long long>(a_bits) << 16) | v_bits;
+            }
+        }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        checked += __shfl_xor_sync(0xffffffffu, checked, o);
+        bad += __shfl_xor_sync(0xffffffffu, bad, o);
+    }
+    if ((threadIdx.x & 31) == 0) {
+        atomicAdd(&out[0], checked);
+        if (bad) atomicAdd(&out[1], bad);
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_quotient_selftest(unsigned long long *out, cudaStream_t stream)
+{
+    cudaError_t e = cudaMemsetAsync(out, 0, 3 * sizeof(unsigned long long), stream);
+    if (e != cudaSuccess) return e;
+    quotient_selftest_kernel<<<0x7F7Fu, 256, 0, stream>>>(out);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_quantize_act(const uint16_t *x, int64_t ldx, int M, int K, int8_t *q, float *s_a, bool pdl,
                                 cudaStream_t stream)

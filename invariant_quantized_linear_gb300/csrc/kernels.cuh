@@ -56,6 +56,7 @@ cudaError_t launch_residual_quantize(uint16_t *h, const uint16_t *y, int64_t ldy
 cudaError_t launch_relu_mul_quantize(const uint16_t *gu, int64_t ldgu, int M, int K, int8_t *q, float *s_a,
                                      uint16_t *m_out, bool pdl, cudaStream_t stream);
 cudaError_t launch_wait_selftest(int *status, cudaStream_t stream);
+cudaError_t launch_quotient_selftest(unsigned long long *out, cudaStream_t stream);
 cudaError_t launch_greedy_verify(const int32_t *argmax, const int32_t *draft, int M, int32_t *out,
                                  cudaStream_t stream);
 cudaError_t launch_quantize_weight(const float *w, int64_t ldw, int N, int K, int8_t *w_q, float *s_w,

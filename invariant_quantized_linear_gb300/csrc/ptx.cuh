@@ -195,40 +195,6 @@ __device__ __forceinline__ void i8x4_to_f16x2x2(uint32_t v, uint32_t &lo, uint32
     asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(h), "r"(bias));
 }
 
-// Per-element activation code clamp(rne(v / s), -127, 127) with v / s an IEEE
-// division, computed as v * r with r = 1/s correctly rounded, and checked.
-// With |v / s| <= 127.0001, the product v * r differs from the rounded
-// quotient fl(v / s) by less than 3 * 2^-24 * 127.0001 < 2.3e-5 (three
-// roundings of relative size <= 2^-24 each), so both round to the same
-// integer unless the product lies within that distance of a half-integer.
-// Products within 2^-15 (3.05e-5) of a half-integer take the exact division
-// instead, about one element in sixteen thousand.
-// The exact path is one out-of-line copy: inlined at every element it would
-// multiply the code of an unrolled row loop for a branch taken about once in
-// sixteen thousand elements.
-static __device__ __noinline__ int quant_code_exact(float v, float s)
-{
-    return __float2int_rn(__fdiv_rn(v, s));
-}
-
-// The rounding to an integer uses fp32 adds, not conversion instructions
-// (which issue at a fraction of the add rate): for |t| < 2^22, t + 1.5 * 2^23
-// lies in [2^23, 2^24), where the fp32 spacing is 1, so the add rounds t to
-// the nearest integer, ties to even, and that integer is the sum's bit
-// pattern minus the pattern of 1.5 * 2^23.  The subtraction back is exact.
-__device__ __forceinline__ int quant_code(float v, float s, float r)
-{
-    constexpr float kMagic = 12582912.0f;   // 1.5 * 2^23, bit pattern 0x4B400000
-    const float t = __fmul_rn(v, r);
-    const float u = __fadd_rn(t, kMagic);
-    const float kf = __fsub_rn(u, kMagic);
-    const float d = fabsf(__fsub_rn(t, kf));   // exact: |t| < 2^8
-    int k = __float_as_int(u) - 0x4B400000;
-    // (also taken when r overflowed for a tiny subnormal s: t is then inf or NaN)
-    if (!(d < 0.5f - 0x1p-15f)) k = quant_code_exact(v, s);
-    return max(-127, min(127, k));
-}
-
 // fp32 holding an integer below 2^24 in magnitude -> int32 (exact).
 __device__ __forceinline__ int32_t f2i_exact(float f)
 {

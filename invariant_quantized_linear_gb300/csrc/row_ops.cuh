@@ -130,4 +130,61 @@ __device__ __forceinline__ uint4 scale8(const uint4 &t, float f)
     return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// Correctly rounded fp32 quotient v / s, given r = RN(1/s), by one
+// fused-multiply-add correction (Markstein's division step; P. Markstein,
+// "Computation of elementary functions on the IBM RISC System/6000
+// processor", IBM J. Res. Dev. 34(1), 1990): q0 = RN(v r) is within one ulp
+// of v / s, the remainder v - q0 s is exact in one fma, and RN(q0 + rem r)
+// is RN(v / s) when nothing underflows.  It is used for rows whose scale s is
+// at least 2^-64, where the remainder of any quotient from 2^-8 up is a
+// normal number; smaller quotients may differ from IEEE division's in their
+// last bits, but round to code 0 either way.  The library's self-test checks
+// codes for every bf16 v and every bf16 row maximum, and quotients from 2^-8
+// up.
+__device__ __forceinline__ float quotient_rn(float v, float s, float r)
+{
+    const float q0 = __fmul_rn(v, r);
+    const float rem = __fmaf_rn(-q0, s, v);
+    return __fmaf_rn(rem, r, q0);
+}
+
+// The smallest row scale whose codes take quotient_rn.
+constexpr float kQuotientMinScale = 0x1p-64f;
+
+// clamp(rne(q), -127, 127) for |q| < 2^22 by one fp32 add: q + 1.5 * 2^23 lies
+// in [2^23, 2^24), where the fp32 spacing is 1, so the add rounds q to the
+// nearest integer, ties to even, and that integer is the sum's bit pattern
+// minus the pattern of 1.5 * 2^23.
+__device__ __forceinline__ uint32_t code_byte(float q)
+{
+    const float u = __fadd_rn(q, 12582912.0f);   // 1.5 * 2^23, bit pattern 0x4B400000
+    return static_cast<uint32_t>(max(-127, min(127, __float_as_int(u) - 0x4B400000))) & 0xFFu;
+}
+
+// Codes clamp(rne(v / s), -127, 127) of one chunk (8 bf16 values), packed as 8
+// bytes in element order; s >= kQuotientMinScale, r = RN(1/s).
+__device__ __forceinline__ uint2 quant8(const uint4 &t, float s, float r)
+{
+    const uint32_t w[4] = {t.x, t.y, t.z, t.w};
+    uint32_t o[2] = {0u, 0u};
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+        o[e >> 1] |= (code_byte(quotient_rn(bf16_lo(w[e]), s, r)) | (code_byte(quotient_rn(bf16_hi(w[e]), s, r)) << 8))
+                     << (16 * (e & 1));
+    return make_uint2(o[0], o[1]);
+}
+
+// The same codes by IEEE division (any s > 0); rows with s below
+// kQuotientMinScale take it.
+__device__ __forceinline__ uint2 quant8_div(const uint4 &t, float s)
+{
+    const uint32_t w[4] = {t.x, t.y, t.z, t.w};
+    uint32_t o[2] = {0u, 0u};
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+        o[e >> 1] |= (code_byte(__fdiv_rn(bf16_lo(w[e]), s)) | (code_byte(__fdiv_rn(bf16_hi(w[e]), s)) << 8))
+                     << (16 * (e & 1));
+    return make_uint2(o[0], o[1]);
+}
+
 }  // namespace bi

@@ -168,3 +168,19 @@ def test_bounded_wait_reports_timeout_and_context_survives(bi):
     wq_o, sw_o = oracle_weights(oracle, gen.weight_f32(5, 0, 0, 64, 256), True)
     assert np.array_equal(to_np(y), oracle.linear_w8a8(q_o, s_o, wq_o, sw_o))
     assert bi.bi_workspace_status(ws) == bi.BI_OK
+
+
+def test_executor_quotient_equals_ieee_division_exhaustively(bi):
+    """The executor quantises with v / s formed from RN(1/s) and one fma
+    correction; over every bf16 row maximum and every bf16 v with |v| <= amax
+    the quotient and the code equal IEEE division's."""
+    out = torch.zeros(3, dtype=torch.int64, device=DEV)
+    bi.bi_selftest_quotient(out)
+    torch.cuda.synchronize()
+    checked, bad, example = (int(t) for t in out.cpu())
+    # every pair of the domain, counted on the host by the same rule
+    a = np.arange(1, 0x7F80, dtype=np.uint32)
+    s = ((a << 16).view(np.float32) / np.float32(127)).astype(np.float32)
+    keep = s >= np.float32(2.0 ** -64)
+    assert checked == int((2 * (a[keep].astype(np.int64) + 1)).sum()), checked
+    assert bad == 0, "%d mismatches, e.g. amax bits %#06x, v bits %#06x" % (bad, example >> 16, example & 0xFFFF)
