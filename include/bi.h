@@ -158,7 +158,11 @@ BI_API bi_status bi_requant_pow2(const int8_t *w_q, const float *s_w, int N, int
  * workspace holds split-K partial sums, their counters and a status word.  It
  * must be zero-filled before its first use (cudaMemset); every call that
  * completes leaves it zero-filled again, so one workspace can serve a whole
- * sequence of calls on one stream.
+ * sequence of calls on one stream.  For M > 16 it is larger (about 12.6 MB):
+ * it also holds the int32 partial sums of prefill tiles split along K to fill
+ * the GPU's last wave (scratch: every call overwrites what it reads) and their
+ * counters (zero between calls).  A workspace of the M <= 16 size still works
+ * for M > 16, without that split (same results).
  */
 BI_API size_t bi_linear_workspace_size(int M, int N, int K);
 

@@ -239,10 +239,9 @@ bi_status bi_requant_pow2(const int8_t *w_q, const float *s_w, int N, int K, int
 
 size_t bi_linear_workspace_size(int M, int N, int K)
 {
-    (void)M;
     (void)N;
     (void)K;
-    return bi::kWsBytes;
+    return M > 16 ? bi::kWsPrefillBytes : bi::kWsBytes;
 }
 
 size_t bi_lmhead_workspace_size(int M, int N, int K)
@@ -266,6 +265,10 @@ bi_status bi_linear_w8a8(const int8_t *q, const float *s_a, int M, int K, const 
     bi::PrefillArgs a;
     a.q = q;
     a.w_q = w_q;
+    // a workspace sized for M <= 16 still works, without splitting tiles
+    const bool tail = ws_bytes >= bi::kWsPrefillBytes;
+    a.tail_acc = tail ? reinterpret_cast<int32_t *>(static_cast<char *>(ws) + bi::kWsTailAccOff) : nullptr;
+    a.tail_cnt = tail ? reinterpret_cast<int *>(static_cast<char *>(ws) + bi::kWsTailCntOff) : nullptr;
     a.s_a = s_a;
     a.s_w = s_w;
     a.y = y;

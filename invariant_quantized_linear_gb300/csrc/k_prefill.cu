@@ -12,7 +12,7 @@
 //
 // CTA tile: 128 tokens (MMA M = TMEM lanes) x 256 weight rows (MMA N = TMEM
 // columns), 64 K per stage.  Roles:
-//   warps 0-7   load the tile's int8 rows from global memory four stages
+//   warps 0-7   load the tile's int8 rows from global memory two stages
 //               ahead (into registers), convert them to f16 and store them
 //               into a ring of K-major, 128-byte-swizzled stages;
 //   warps 8-11  TMEM lane quarters 0-3: move chunk sums into the int32
@@ -39,7 +39,6 @@ constexpr int kTileN = 256;                       // weight rows per tile: MMA N
 constexpr int kStepK = 64;                        // K per stage: one 128-byte f16 row
 constexpr int kStages = 4;
 constexpr int kChunkSteps = 16;                   // 1024 K per exact fp32 chunk
-constexpr int kAhead = 4;                         // converter loads run this many steps ahead
 constexpr int kConvWarps = 8;
 constexpr int kConvThreads = kConvWarps * 32;
 constexpr int kEpiWarp0 = kConvWarps;             // warps 8 .. 11 (warp % 4 = lane quarter)
@@ -65,6 +64,11 @@ struct Params {
     int M, N, K;
     int kt;              // K steps
     int vec_y;           // y rows allow 16-byte stores
+    int tiles_m;         // token tiles (tile t: token tile t % tiles_m, weight tile t / tiles_m)
+    int full_tiles;      // tiles 0 .. full_tiles - 1 run whole, one per CTA
+    int parts;           // every later tile runs as `parts` K ranges, one per CTA
+    int32_t *tail_acc;   // per split tile: parts - 1 slots of int32 [256 columns][128 rows] (scratch)
+    int *tail_cnt;       // per split tile: arrivals and K ranges stored, zero between calls
     Workspace ws;
     int pdl;
 };
@@ -83,6 +87,9 @@ __device__ __forceinline__ void store_f16_row(uint8_t *row_base, int row, int c,
     *reinterpret_cast<uint4 *>(row_base + (((2 * c + 1) ^ sw) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
 }
 
+// kSplit = false: tiles 0 .. full_tiles - 1, whole.  kSplit = true: the
+// later tiles, each as `parts` K ranges (one CTA per range), launched after.
+template <bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(Params p)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -95,10 +102,22 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(Params p)
     uint64_t *drain = acc_empty + 1;                                              // all MMAs complete
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    volatile int *last_part = abort_flag + 1;                                     // split tile: arrival ticket
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int m0 = blockIdx.x * kTileM;
-    const int n0 = blockIdx.y * kTileN;
+    // this CTA's tile and K range: whole tiles first, then the split tiles'
+    // ranges (tiles are numbered token tile fastest, so the CTAs resident
+    // together share weight tiles in L2)
+    int tile = static_cast<int>(blockIdx.x), part = 0, parts = 1;
+    if constexpr (kSplit) {
+        tile = p.full_tiles + static_cast<int>(blockIdx.x) / p.parts;
+        part = static_cast<int>(blockIdx.x) % p.parts;
+        parts = p.parts;
+    }
+    const int m0 = (tile % p.tiles_m) * kTileM;
+    const int n0 = (tile / p.tiles_m) * kTileN;
+    const int kb = static_cast<int>(static_cast<long long>(p.kt) * part / parts);   // first K step
+    const int nsteps = static_cast<int>(static_cast<long long>(p.kt) * (part + 1) / parts) - kb;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -127,12 +146,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(Params p)
 
     if (warp < kConvWarps) {
         // ------------------------------------------------ int8 -> f16 stages
+        // (the split tiles' epilogue needs registers: fewer loads in flight)
+        constexpr int kAhead = kSplit ? 2 : 4;
         const int t = threadIdx.x;
         const int c = t & 3;        // 16-byte chunk of the 64-byte int8 row slice
         const int r0 = t >> 2;      // rows r0 + 64 i
         if (p.pdl) pdl_wait();
         auto load = [&](int j, uint4 (&ra)[kChunksA], uint4 (&rb)[kChunksB]) {
-            const int k = j * kStepK + 16 * c;
+            const int k = (kb + j) * kStepK + 16 * c;
             const bool kin = k < p.K;
 #pragma unroll
             for (int i = 0; i < kChunksA; ++i) {
@@ -164,22 +185,29 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(Params p)
             fence_proxy_async_smem();   // the tensor core reads the stage through the async proxy
             __syncwarp();
             if (lane == 0) mbar_arrive(&full[s]);
-            if (j + kAhead < p.kt) load(j + kAhead, ra, rb);
+            if (j + kAhead < nsteps) load(j + kAhead, ra, rb);
             return true;
         };
         // kAhead register sets: the loads of step j + kAhead are issued when
         // step j is stored, which covers the L2 latency under load
         uint4 ra0[kChunksA], rb0[kChunksB], ra1[kChunksA], rb1[kChunksB];
-        uint4 ra2[kChunksA], rb2[kChunksB], ra3[kChunksA], rb3[kChunksB];
         load(0, ra0, rb0);
-        if (p.kt > 1) load(1, ra1, rb1);
-        if (p.kt > 2) load(2, ra2, rb2);
-        if (p.kt > 3) load(3, ra3, rb3);
-        for (int j = 0; j < p.kt; j += kAhead) {
-            if (!step(j, ra0, rb0)) break;
-            if (j + 1 < p.kt && !step(j + 1, ra1, rb1)) break;
-            if (j + 2 < p.kt && !step(j + 2, ra2, rb2)) break;
-            if (j + 3 < p.kt && !step(j + 3, ra3, rb3)) break;
+        if (nsteps > 1) load(1, ra1, rb1);
+        if constexpr (kAhead == 4) {
+            uint4 ra2[kChunksA], rb2[kChunksB], ra3[kChunksA], rb3[kChunksB];
+            if (nsteps > 2) load(2, ra2, rb2);
+            if (nsteps > 3) load(3, ra3, rb3);
+            for (int j = 0; j < nsteps; j += 4) {
+                if (!step(j, ra0, rb0)) break;
+                if (j + 1 < nsteps && !step(j + 1, ra1, rb1)) break;
+                if (j + 2 < nsteps && !step(j + 2, ra2, rb2)) break;
+                if (j + 3 < nsteps && !step(j + 3, ra3, rb3)) break;
+            }
+        } else {
+            for (int j = 0; j < nsteps; j += 2) {
+                if (!step(j, ra0, rb0)) break;
+                if (j + 1 < nsteps && !step(j + 1, ra1, rb1)) break;
+            }
         }
     } else {
         // ------------------------------------------------ MMA issue, chunk moves, epilogue
@@ -194,7 +222,36 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(Params p)
         const int tok = m0 + 32 * qd + lane;
         const float sa = tok < p.M ? p.s_a[tok] : 0.0f;
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * qd) << 16);
-        const int nch = (p.kt + kChunkSteps - 1) / kChunkSteps;
+        uint16_t *yr = p.y + static_cast<size_t>(tok < p.M ? tok : 0) * p.N;
+        // bf16_rne((float(acc) * s_a) * s_w) of 32 columns of this thread's
+        // token row, stored to y
+        auto store_y = [&](int col, const uint32_t (&tot)[32]) {
+            if (tok >= p.M) return;
+            uint32_t o[16];
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+                uint32_t b2 = 0;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    float f = __int2float_rn(static_cast<int32_t>(tot[e + h]));
+                    f = __fmul_rn(f, sa);
+                    f = __fmul_rn(f, sw_tile[col + e + h]);
+                    b2 |= static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(f))) << (16 * h);
+                }
+                o[e >> 1] = b2;
+            }
+            const int n = n0 + col;
+            if (p.vec_y && n + 32 <= p.N) {
+#pragma unroll
+                for (int v = 0; v < 4; ++v)
+                    *reinterpret_cast<uint4 *>(yr + n + 8 * v) = make_uint4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                    if (n + e < p.N) yr[n + e] = static_cast<uint16_t>(o[e >> 1] >> (16 * (e & 1)));
+            }
+        };
+        const int nch = (nsteps + kChunkSteps - 1) / kChunkSteps;
         constexpr uint32_t idesc = tc::idesc_f16_f32(kTileM, kTileN);
         int j = 0;
         for (int ch = 0; ch < nch; ++ch) {
@@ -205,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(Params p)
                     ok = __all_sync(0xffffffffu, mbar_wait_bounded(acc_empty, (ch - 1) & 1, abort_flag));
                     tc::fence_after();
                 }
-                const int jend = min(p.kt, (ch + 1) * kChunkSteps);
+                const int jend = min(nsteps, (ch + 1) * kChunkSteps);
                 for (; ok && j < jend; ++j) {
                     const int s = j % kStages;
                     ok = __all_sync(0xffffffffu, mbar_wait_bounded(&full[s], (j / kStages) & 1, abort_flag));
@@ -253,8 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(Params p)
                 tc::fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(acc_empty);
-            } else {
-                uint16_t *yr = p.y + static_cast<size_t>(tok < p.M ? tok : 0) * p.N;
+            } else if constexpr (!kSplit) {
 #pragma unroll 1
                 for (int col = 0; col < kTileN; col += 32) {
                     uint32_t d[32], tot[32];
@@ -290,6 +346,82 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(Params p)
                             if (n + e < p.N) yr[n + e] = static_cast<uint16_t>(o[e >> 1] >> (16 * (e & 1)));
                     }
                 }
+            } else {
+                // A split tile.  Each K range takes an arrival ticket.  The
+                // first parts - 1 arrivals store their sums into the tile's
+                // slots (one per ticket, column-major so that a warp's stores
+                // cover contiguous rows) and count themselves done; the last
+                // arrival keeps its own sums in TMEM, waits until the others
+                // are done (they are running: they arrived first), adds their
+                // slots and applies the epilogue.  Integer adds in any order
+                // give the same exact sum.
+                const int ti = tile - p.full_tiles;
+                int *arrive = p.tail_cnt + 2 * ti, *done = arrive + 1;
+                const size_t slot0 = static_cast<size_t>(ti) * (parts - 1);
+                const int row = 32 * qd + lane;
+                if (et == 0) *last_part = atomicAdd(arrive, 1);
+                asm volatile("bar.sync 1, 128;" ::: "memory");
+                const int ticket = *last_part;
+                if (ticket < parts - 1) {
+                    int32_t *dst = p.tail_acc + (slot0 + ticket) * (kTileN * kTileM) + row;
+#pragma unroll 1
+                    for (int col = 0; col < kTileN; col += 32) {
+                        uint32_t d[32], tot[32];
+                        tc::ld32(lane_addr + col, d);
+                        if (ch > 0) tc::ld32(lane_addr + kTotCol + col, tot);
+                        tc::wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) {
+                            int32_t v = f2i_exact(__uint_as_float(d[e]));
+                            if (ch > 0) v += static_cast<int32_t>(tot[e]);
+                            __stcg(dst + (col + e) * kTileM, v);
+                        }
+                    }
+                    __threadfence();
+                    asm volatile("bar.sync 1, 128;" ::: "memory");
+                    if (et == 0) red_release_gpu_add(done, 1);
+                } else {
+                    if (et == 0) {
+                        const unsigned long long t0 = global_timer_ns();
+                        int spins = 0;
+                        while (ld_acquire_gpu(done) < parts - 1) {
+                            __nanosleep(64);
+                            if ((++spins & 63) == 0 && (*abort_flag || global_timer_ns() - t0 > kWaitLimitNs)) {
+                                fail();
+                                break;
+                            }
+                        }
+                    }
+                    asm volatile("bar.sync 1, 128;" ::: "memory");
+                    if (!*abort_flag) {
+                        const int32_t *src = p.tail_acc + slot0 * (kTileN * kTileM) + row;
+#pragma unroll 1
+                        for (int col = 0; col < kTileN; col += 32) {
+                            uint32_t d[32], tot[32];
+                            __syncwarp();   // reconverge after the ragged stores of the previous columns
+                            tc::ld32(lane_addr + col, d);
+                            if (ch > 0) tc::ld32(lane_addr + kTotCol + col, tot);
+                            tc::wait_ld();
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) {
+                                const int32_t v = f2i_exact(__uint_as_float(d[e]));
+                                tot[e] = ch > 0 ? static_cast<uint32_t>(static_cast<int32_t>(tot[e]) + v)
+                                                : static_cast<uint32_t>(v);
+                            }
+#pragma unroll 1
+                            for (int o = 0; o < parts - 1; ++o)
+#pragma unroll
+                                for (int e = 0; e < 32; ++e)
+                                    tot[e] += static_cast<uint32_t>(
+                                        __ldcg(src + static_cast<size_t>(o) * (kTileN * kTileM) + (col + e) * kTileM));
+                            store_y(col, tot);
+                        }
+                        if (et == 0) {
+                            *arrive = 0;
+                            *done = 0;
+                        }
+                    }
+                }
             }
         }
         __syncwarp();
@@ -316,8 +448,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(Params p)
 cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream)
 {
     static bool attr_set = false;
+    static int sms = 0;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        cudaError_t e = cudaFuncSetAttribute(prefill_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(prefill_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        if (e != cudaSuccess) return e;
+        int dev = 0;
+        e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
@@ -334,9 +474,25 @@ cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream)
     p.vec_y = ((a.N % 8) == 0 && (reinterpret_cast<uintptr_t>(a.y) & 15u) == 0) ? 1 : 0;
     p.ws = a.ws;
     p.pdl = a.pdl ? 1 : 0;
+    // One CTA per SM.  Tiles that fill whole waves run whole; when the last
+    // wave would be at most half full, its tiles are split along K into as
+    // many ranges (of at least 8 steps) as fill it, within the scratch slots.
+    p.tiles_m = (a.M + kTileM - 1) / kTileM;
+    const int tiles = p.tiles_m * ((a.N + kTileN - 1) / kTileN);
+    p.full_tiles = tiles;
+    p.parts = 1;
+    p.tail_acc = a.tail_acc;
+    p.tail_cnt = a.tail_cnt;
+    const int rem = sms > 0 ? tiles % sms : 0;
+    if (a.tail_acc && rem > 0 && rem <= sms / 2 && rem <= kMaxTailTiles) {
+        // ranges of at least 8 steps; rem * (parts - 1) slots of scratch
+        const int parts = min(min(sms / rem, p.kt / 8), 1 + kMaxTailSlots / rem);
+        if (parts >= 2) {
+            p.full_tiles = tiles - rem;
+            p.parts = parts;
+        }
+    }
     cudaLaunchConfig_t cfg = {};
-    // token tiles fastest: the CTAs resident together share weight tiles in L2
-    cfg.gridDim = dim3(static_cast<unsigned>((a.M + kTileM - 1) / kTileM), static_cast<unsigned>((a.N + kTileN - 1) / kTileN));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = stream;
@@ -344,8 +500,19 @@ cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream)
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = a.pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, prefill_kernel, p);
+    if (p.full_tiles > 0) {
+        cfg.gridDim = dim3(static_cast<unsigned>(p.full_tiles));
+        cfg.numAttrs = a.pdl ? 1 : 0;
+        const cudaError_t e = cudaLaunchKernelEx(&cfg, prefill_kernel<false>, p);
+        if (e != cudaSuccess || p.full_tiles == tiles) return e;
+    }
+    // The split tiles, after the whole ones: a programmatic dependent whose
+    // CTAs wait (griddepcontrol.wait) for everything before them, so they
+    // take the SMs as the whole tiles finish.
+    cfg.gridDim = dim3(static_cast<unsigned>((tiles - p.full_tiles) * p.parts));
+    cfg.numAttrs = (a.pdl || p.full_tiles > 0) ? 1 : 0;
+    p.pdl = cfg.numAttrs;
+    return cudaLaunchKernelEx(&cfg, prefill_kernel<true>, p);
 }
 
 }  // namespace bi

@@ -93,18 +93,6 @@ struct PCfg {
     static constexpr int kSmemBytes = kStages * (kWStage + kAStage) + kRedBytes + kDeferBytes + 1024 + kCtlBytes;
 };
 
-__device__ __forceinline__ int ld_acquire_gpu(const int *p)
-{
-    int v;
-    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ void red_release_gpu_add(int *p, int v)
-{
-    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
 // Order this thread's earlier generic-proxy global writes (or, on the reading
 // side, its acquire) with async-proxy (TMA) accesses to global memory.
 __device__ __forceinline__ void fence_proxy_async_global()

@@ -27,6 +27,16 @@ constexpr size_t kWsBestOff = kWsCounterOff + sizeof(int32_t) * kMaxGrid;
 constexpr size_t kWsPartialOff = kWsBestOff + sizeof(unsigned long long) * kMaxGrid * kMaxTok;
 constexpr size_t kWsBytes = kWsPartialOff + sizeof(int32_t) * kMaxGrid * kBM * kMaxTok;
 
+// Prefill (M > 16) workspaces append, after kWsBytes, the partial sums of
+// tiles split along K (the leftover of the last wave): kMaxTailSlots slots of
+// int32 [256][128] (scratch, overwritten before it is read), then two
+// counters per split tile (zero between calls, like the rest).
+constexpr int kMaxTailTiles = 96;
+constexpr int kMaxTailSlots = 96;
+constexpr size_t kWsTailAccOff = kWsBytes;
+constexpr size_t kWsTailCntOff = kWsTailAccOff + sizeof(int32_t) * kMaxTailSlots * 256 * 128;
+constexpr size_t kWsPrefillBytes = kWsTailCntOff + 256 * ((2 * sizeof(int32_t) * kMaxTailTiles + 255) / 256);
+
 struct Workspace {
     int *status;                 // DEV_OK / DEV_TIMEOUT
     int *ticket;                 // CTAs finished (argmax)
@@ -83,6 +93,8 @@ cudaError_t launch_skinny(const SkinnyArgs &a, cudaStream_t stream);
 struct PrefillArgs {
     const int8_t *q;           // [M, K], rows 16-byte aligned
     const int8_t *w_q;         // [N, K], rows 16-byte aligned
+    int32_t *tail_acc;         // split-tile sums (null: no tile is split)
+    int *tail_cnt;             // split-tile counters
     const float *s_a;
     const float *s_w;
     uint16_t *y;

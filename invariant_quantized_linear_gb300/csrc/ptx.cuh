@@ -211,6 +211,20 @@ __device__ __forceinline__ int atom_add_acq_rel_gpu(int *p, int v)
     return old;
 }
 
+// Load with acquire / add with release semantics, at GPU scope: a flag or
+// counter that other CTAs of the grid update.
+__device__ __forceinline__ int ld_acquire_gpu(const int *p)
+{
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void red_release_gpu_add(int *p, int v)
+{
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 // ------------------------------------------------ programmatic dependent launch
 
 // Wait until the grids this one depends on have completed and their memory

@@ -85,6 +85,27 @@ def test_rows_are_batch_invariant(bi, N, K):
         assert torch.equal(y, single[:M]), M
 
 
+def test_prefill_split_tiles_leave_workspace_zeroed(bi):
+    """M = 200, N = 1000, K = 4096: 8 tiles on the GPU's SMs are split along K
+    (the last wave is less than half full); the split tiles' counters return
+    to zero (their partial-sum slots are scratch), and a workspace sized for
+    M <= 16 (no split) gives the same bits."""
+    M, N, K = 200, 1000, 4096
+    x_np, w = _case(13, M, N, K, True)
+    wq, sw = weights(bi, w, pow2=True)
+    q, s = quant_act(bi, x_np)
+    ws = bi.new_workspace(M, N, K)
+    assert ws.numel() > bi.new_workspace(16, N, K).numel()
+    ys = [linear(bi, q, s, wq, sw, ws=ws) for _ in range(3)]
+    y_small = linear(bi, q, s, wq, sw, ws=bi.new_workspace(16, N, K))
+    torch.cuda.synchronize()
+    assert all(torch.equal(y, y_small) for y in ys)
+    small = bi.new_workspace(16, N, K).numel()
+    slots = 96 * 256 * 128 * 4
+    assert int(ws[:small].count_nonzero()) == 0 and int(ws[small + slots:].count_nonzero()) == 0
+    assert bi.bi_workspace_status(ws) == bi.BI_OK
+
+
 def test_pdl_flag_and_graph_capture_same_bits(bi):
     """PDL launches, and a CUDA graph of quantise + linear with PDL, give the
     same bits as plain launches."""
