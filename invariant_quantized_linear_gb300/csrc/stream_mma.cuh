@@ -52,13 +52,15 @@ __device__ __forceinline__ unsigned long long argmax_key(uint16_t b, int n)
 
 // Which 32-byte groups of K run on the int8 MMA (no conversion; a separate,
 // slower pipe) and which on the f16 MMA (fast, but each int8 operand is first
-// converted): splitting the groups keeps both pipes and the ALU below their
-// limits at HBM speed.  With two token tiles the int8 MMA does twice the work
-// per group, so it takes a smaller share.
+// converted).  Measured on the 36-layer verify pass: with one token tile every
+// group on the int8 MMA is fastest (2.31 ms against 2.36 with half and 2.44
+// with a quarter: the conversions cost more than the int8 pipe's rate); with
+// two token tiles, where the int8 MMA does twice the work per group, the share
+// made no difference, and a quarter is kept.
 template <int MT>
 __device__ __forceinline__ constexpr bool imma_group(int t)
 {
-    return MT == 1 ? (t & 1) == 0 : (t & 3) == 0;
+    return MT == 1 ? true : (t & 3) == 0;
 }
 
 // Lane constants of a consumer warp for ldmatrix and the MMA fragments.
