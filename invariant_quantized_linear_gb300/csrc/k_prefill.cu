@@ -408,12 +408,26 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(Params p)
                                 tot[e] = ch > 0 ? static_cast<uint32_t>(static_cast<int32_t>(tot[e]) + v)
                                                 : static_cast<uint32_t>(v);
                             }
+                            // two slots per round trip: 64 loads in flight
+                            const int32_t *sc = src + col * kTileM;
+                            int o = 0;
 #pragma unroll 1
-                            for (int o = 0; o < parts - 1; ++o)
+                            for (; o + 1 < parts - 1; o += 2) {
+                                int32_t l0[32], l1[32];
+#pragma unroll
+                                for (int e = 0; e < 32; ++e) {
+                                    l0[e] = __ldcg(sc + static_cast<size_t>(o) * (kTileN * kTileM) + e * kTileM);
+                                    l1[e] = __ldcg(sc + static_cast<size_t>(o + 1) * (kTileN * kTileM) + e * kTileM);
+                                }
+#pragma unroll
+                                for (int e = 0; e < 32; ++e) tot[e] += static_cast<uint32_t>(l0[e] + l1[e]);
+                            }
+                            if (o < parts - 1) {
 #pragma unroll
                                 for (int e = 0; e < 32; ++e)
                                     tot[e] += static_cast<uint32_t>(
-                                        __ldcg(src + static_cast<size_t>(o) * (kTileN * kTileM) + (col + e) * kTileM));
+                                        __ldcg(sc + static_cast<size_t>(o) * (kTileN * kTileM) + e * kTileM));
+                            }
                             store_y(col, tot);
                         }
                         if (et == 0) {
