@@ -11,10 +11,12 @@
 // of TMEM, before the next chunk starts.
 //
 // CTA tile: 128 tokens (MMA M = TMEM lanes) x 256 weight rows (MMA N = TMEM
-// columns), 64 K per stage.  Roles:
-//   warps 0-7   load the tile's int8 rows from global memory two stages
-//               ahead (into registers), convert them to f16 and store them
-//               into a ring of K-major, 128-byte-swizzled stages;
+// columns), 64 K per stage, one CTA per SM.  Roles:
+//   warps 0-7   load the tile's int8 rows from global memory four stages
+//               ahead (two in split tiles) into registers, convert them to
+//               f16, store them into a ring of K-major, 128-byte-swizzled
+//               stages and arrive on the stage's barrier (one arrival per
+//               warp);
 //   warps 8-11  TMEM lane quarters 0-3: move chunk sums into the int32
 //               totals, then the epilogue, one token row per thread; warp 8
 //               also allocates TMEM, and its lane 0 issues the MMAs and
@@ -22,6 +24,13 @@
 //               chunk's move in any case).
 // Loading through registers rather than TMA keeps the int8 bytes out of
 // shared memory, whose bandwidth the MMA operands and the f16 stores share.
+//
+// Tiles that fill whole waves run whole (prefill_kernel<false>).  When the
+// last wave would be at most half full, its tiles run in a second launch
+// (prefill_kernel<true>), each split along K into ranges whose int32 sums
+// meet in workspace slots; the range that arrives last adds them and applies
+// the epilogue.  Integer sums are exact in any order, so the bits do not
+// depend on the split.
 // Every wait is bounded: on a timeout the kernel writes DEV_TIMEOUT to the
 // workspace status word and every role returns.
 #include "kernels.cuh"
