@@ -44,6 +44,14 @@ def lib():
         L.oracle_relu_mul.restype = None
         L.oracle_greedy_verify.argtypes = [vp, vp, ci, vp]
         L.oracle_greedy_verify.restype = None
+        L.oracle_quantize_q6.argtypes = [vp, ci, ci, vp, vp, vp, vp]
+        L.oracle_quantize_q6.restype = None
+        L.oracle_q6_code.argtypes = [vp, vp, ci, ci, ci]
+        L.oracle_q6_code.restype = ci
+        L.oracle_quantize_act_blocks.argtypes = [vp, i64, ci, ci, vp, vp]
+        L.oracle_quantize_act_blocks.restype = None
+        L.oracle_linear_q6.argtypes = [vp, vp, ci, ci, vp, vp, vp, vp, ci, vp]
+        L.oracle_linear_q6.restype = None
         L.oracle_num_threads.argtypes = []
         L.oracle_num_threads.restype = ci
         _LIB = L
@@ -209,6 +217,55 @@ def greedy_verify(argmax: np.ndarray, draft: np.ndarray):
     out = np.empty(2, np.int32)
     lib().oracle_greedy_verify(am.ctypes.data, d.ctypes.data, M, out.ctypes.data)
     return int(out[0]), int(out[1])
+
+
+# ------------------------------------------------------------ block-scaled variant
+# ("why speculative decoding changed my output", "the mat-vec kernel"; the
+# format and the fixed order of adds are defined in oracle.c)
+
+def quantize_q6(w_f32: np.ndarray):
+    """fp32 W [N, K] (K % 256 == 0) -> (ql uint8 [N, K/2], qh uint8 [N, K/4],
+    sc int8 [N, K/16], d fp32 [N, K/256])."""
+    w = _c(w_f32, np.float32)
+    N, K = w.shape
+    assert K % 256 == 0
+    ql = np.zeros((N, K // 2), np.uint8)
+    qh = np.zeros((N, K // 4), np.uint8)
+    sc = np.zeros((N, K // 16), np.int8)
+    d = np.zeros((N, K // 256), np.float32)
+    lib().oracle_quantize_q6(w.ctypes.data, N, K, ql.ctypes.data, qh.ctypes.data, sc.ctypes.data, d.ctypes.data)
+    return ql, qh, sc, d
+
+
+def q6_codes(ql: np.ndarray, qh: np.ndarray) -> np.ndarray:
+    """The int8 codes [N, K] of a block-scaled matrix, one call per element."""
+    ql, qh = _c(ql, np.uint8), _c(qh, np.uint8)
+    N, K = ql.shape[0], 2 * ql.shape[1]
+    L = lib()
+    return np.array([[L.oracle_q6_code(ql.ctypes.data, qh.ctypes.data, K, n, k) for k in range(K)]
+                     for n in range(N)], np.int8)
+
+
+def quantize_act_blocks(x_bf16: np.ndarray):
+    """bf16 x [M, K] (uint16 patterns, K % 32 == 0) -> (q int8 [M, K], d_a fp32 [M, K/32])."""
+    x = _c(x_bf16, np.uint16)
+    M, K = x.shape
+    q = np.empty((M, K), np.int8)
+    d = np.empty((M, K // 32), np.float32)
+    lib().oracle_quantize_act_blocks(x.ctypes.data, K, M, K, q.ctypes.data, d.ctypes.data)
+    return q, d
+
+
+def linear_q6(qa, d_a, ql, qh, sc, d) -> np.ndarray:
+    """y fp32 [M, N] of the block-scaled linear, in the fixed order of adds."""
+    qa, d_a = _c(qa, np.int8), _c(d_a, np.float32)
+    ql, qh, sc, d = _c(ql, np.uint8), _c(qh, np.uint8), _c(sc, np.int8), _c(d, np.float32)
+    M, K = qa.shape
+    N = ql.shape[0]
+    y = np.empty((M, N), np.float32)
+    lib().oracle_linear_q6(qa.ctypes.data, d_a.ctypes.data, M, K, ql.ctypes.data, qh.ctypes.data, sc.ctypes.data,
+                           d.ctypes.data, N, y.ctypes.data)
+    return y
 
 
 def num_threads() -> int:

@@ -337,6 +337,136 @@ void oracle_greedy_verify(const int32_t *argmax, const int32_t *draft, int M, in
     out[1] = argmax[L];
 }
 
+/* ------------------------------------------------ block-scaled variant
+ *
+ * The mat-vec of [cintu] "the mat-vec kernel": a weight row of K inputs is cut
+ * into blocks of 256 weights, the activations into int8 blocks of 32; the
+ * products inside a block are integer (exact in any order), and each block's
+ * integer result is scaled and added into an fp32 accumulator, whose order
+ * of adds must be the same for every number of tokens in the pass.
+ *
+ * The pages name the formats (q6_k weights, int8 activation blocks of 32) but
+ * print no layout and no quantiser, so this library defines its own:
+ *  - weights: super-blocks of 256 = 16 sub-blocks of 16.  Code c in [-32, 31]
+ *    (6 bits), int8 sub-scale sc per sub-block, fp32 scale d per super-block;
+ *    w ~ c * (d * sc).  Stored as ql [N][K/2] (low 4 bits of c + 32; element k
+ *    in byte k/2, bits 4 * (k & 1)), qh [N][K/4] (high 2 bits of c + 32;
+ *    element k in byte k/4, bits 2 * (k & 3)), sc [N][K/16], d [N][K/256].
+ *  - quantiser, per super-block: t_j = absmax_j / 31 (fp32 division) for each
+ *    sub-block j; d = max_j t_j / 127 (1 if all zero); sc_j = clamp(rne(t_j /
+ *    d), 0, 127); e_j = d * sc_j (fp32); c = clamp(rne(w / e_j), -32, 31), or 0
+ *    when e_j = 0.
+ *  - activations: blocks of 32 with the per-token rule of A1 applied to each
+ *    block: d_a = absmax / 127 (1 if zero), q = clamp(rne(x / d_a), +-127).
+ *  - the sum: 32-block b (of K / 32) of super-block s = b / 8 holds sub-blocks
+ *    j = 16 s + 2 (b % 8) and j + 1; isum_b = sc_j * sum(c * q) over its first
+ *    16 elements + sc_(j+1) * sum over the next 16 (|isum| < 2^24, exact in
+ *    fp32); contribution v_b = ((float)isum_b * d_a[b]) * d[s].  Lane l
+ *    (0..31) adds v_l, v_(l+32), v_(l+64), ... in that order into a partial
+ *    starting at +0; then, for offsets 16, 8, 4, 2, 1, every partial becomes
+ *    p[l] + p[l xor offset]; y = p[0] (fp32, not rounded further).  The order
+ *    depends on K only, so every token of every pass gets the same adds.
+ */
+static float rne_f(double v) { return (float)rne_to_int(v); }
+
+void oracle_quantize_q6(const float *w, int N, int K, uint8_t *ql, uint8_t *qh, int8_t *sc, float *d)
+{
+#pragma omp parallel for schedule(static)
+    for (int n = 0; n < N; ++n) {
+        const float *wr = w + (int64_t)n * K;
+        for (int s = 0; s < K / 256; ++s) {
+            float t[16], tmax = 0.0f;
+            for (int j = 0; j < 16; ++j) {
+                float amax = 0.0f;
+                for (int i = 0; i < 16; ++i) {
+                    float a = fabsf(wr[256 * s + 16 * j + i]);
+                    if (a > amax) amax = a;
+                }
+                t[j] = amax / 31.0f;
+                if (t[j] > tmax) tmax = t[j];
+            }
+            float ds = (tmax == 0.0f) ? 1.0f : tmax / 127.0f;
+            d[(int64_t)n * (K / 256) + s] = ds;
+            for (int j = 0; j < 16; ++j) {
+                float r = rne_f((double)(t[j] / ds));
+                if (r > 127.0f) r = 127.0f;
+                if (r < 0.0f) r = 0.0f;
+                int8_t scj = (int8_t)r;
+                sc[(int64_t)n * (K / 16) + 16 * s + j] = scj;
+                float e = ds * (float)scj;
+                for (int i = 0; i < 16; ++i) {
+                    int64_t k = 256 * s + 16 * j + i;
+                    int c = 0;
+                    if (e != 0.0f) {
+                        float v = rne_f((double)(wr[k] / e));
+                        if (v > 31.0f) v = 31.0f;
+                        if (v < -32.0f) v = -32.0f;
+                        c = (int)v;
+                    }
+                    unsigned u = (unsigned)(c + 32);
+                    uint8_t *bl = &ql[(int64_t)n * (K / 2) + k / 2];
+                    uint8_t *bh = &qh[(int64_t)n * (K / 4) + k / 4];
+                    if ((k & 1) == 0) *bl = (uint8_t)((*bl & 0xF0u) | (u & 0xFu));
+                    else *bl = (uint8_t)((*bl & 0x0Fu) | ((u & 0xFu) << 4));
+                    unsigned sh = 2u * (unsigned)(k & 3);
+                    *bh = (uint8_t)((*bh & ~(3u << sh)) | (((u >> 4) & 3u) << sh));
+                }
+            }
+        }
+    }
+}
+
+/* The code of weight k in row n of a block-scaled matrix (layout above). */
+int oracle_q6_code(const uint8_t *ql, const uint8_t *qh, int K, int n, int k)
+{
+    unsigned lo = (ql[(int64_t)n * (K / 2) + k / 2] >> (4 * (k & 1))) & 0xFu;
+    unsigned hi = (qh[(int64_t)n * (K / 4) + k / 4] >> (2 * (k & 3))) & 3u;
+    return (int)(lo | (hi << 4)) - 32;
+}
+
+void oracle_quantize_act_blocks(const uint16_t *x, int64_t ldx, int M, int K, int8_t *q, float *d_a)
+{
+    float row[32];
+    for (int m = 0; m < M; ++m)
+        for (int b = 0; b < K / 32; ++b) {
+            for (int i = 0; i < 32; ++i)
+                row[i] = oracle_bf16_to_f32(x[(int64_t)m * ldx + 32 * b + i]);
+            quantize_row_f32(row, 32, q + (int64_t)m * K + 32 * b, &d_a[(int64_t)m * (K / 32) + b]);
+        }
+}
+
+void oracle_linear_q6(const int8_t *qa, const float *d_a, int M, int K, const uint8_t *ql, const uint8_t *qh,
+                      const int8_t *sc, const float *d, int N, float *y)
+{
+    const int nb = K / 32;
+#pragma omp parallel for schedule(static)
+    for (int n = 0; n < N; ++n)
+        for (int m = 0; m < M; ++m) {
+            float p[32];
+            for (int l = 0; l < 32; ++l) {
+                p[l] = 0.0f;
+                for (int b = l; b < nb; b += 32) {
+                    int s = b / 8, j = 16 * s + 2 * (b % 8);
+                    int64_t part[2] = {0, 0};
+                    for (int i = 0; i < 32; ++i) {
+                        int k = 32 * b + i;
+                        part[i / 16] += (int64_t)oracle_q6_code(ql, qh, K, n, k) * qa[(int64_t)m * K + k];
+                    }
+                    int64_t isum = (int64_t)sc[(int64_t)n * (K / 16) + j] * part[0] +
+                                   (int64_t)sc[(int64_t)n * (K / 16) + j + 1] * part[1];
+                    float v = ((float)isum * d_a[(int64_t)m * nb + b]) * d[(int64_t)n * (K / 256) + s];
+                    p[l] = p[l] + v;
+                }
+            }
+            for (int off = 16; off > 0; off /= 2) {
+                float q2[32];
+                for (int l = 0; l < 32; ++l) q2[l] = p[l] + p[l ^ off];
+                memcpy(p, q2, sizeof(p));
+            }
+            y[(int64_t)m * N + n] = p[0];
+        }
+}
+
 /* Number of OpenMP threads the parallel loops above use (1 without OpenMP). */
 int oracle_num_threads(void)
 {
