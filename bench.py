@@ -67,6 +67,8 @@ def parse():
     p.add_argument("--no-sweep", action="store_true", help="skip the per-M sweep")
     p.add_argument("--prefill-only", type=int, default=0, metavar="M",
                    help="time only the prefill contraction at M tokens and print its figures")
+    p.add_argument("--blockq-only", action="store_true",
+                   help="time only the block-scaled variant and print its figures")
     p.add_argument("--mode", default="program", choices=["program", "calls"],
                    help="program: the step as one verify-pass program launch; calls: one launch per op")
     return p.parse_args()
@@ -347,6 +349,52 @@ def prefill_measure(bi, torch, st, stream, peaks, Ms=(512, 2048)):
     return out
 
 
+def blockq_measure(bi, torch, dev, stream, peaks, Ms=(1, 8, 16)):
+    """The block-scaled variant (q6-style weight blocks of 256, int8 activation
+    blocks of 32, fixed fp32 order) on layer 0's gate/up shape (N = 24576,
+    K = 4096) through bi_linear_q6, timed alone: stored weight bytes (codes,
+    sub-scales, super-block scales) per second.  Four quantised copies of the
+    weights rotate, so each call reads its weights from HBM, not L2."""
+    import gen
+    N, K, copies = 24576, 4096, 4
+    w = torch.from_numpy(gen.weight_f32(gen.STACK36.seed, 0, 0, N, K)).to(dev)
+    Ws = []
+    for c in range(copies):
+        ql = torch.empty((N, K // 2), dtype=torch.uint8, device=dev)
+        qh = torch.empty((N, K // 4), dtype=torch.uint8, device=dev)
+        sc = torch.empty((N, K // 16), dtype=torch.int8, device=dev)
+        d = torch.empty((N, K // 256), dtype=torch.float32, device=dev)
+        bi.bi_quantize_weight_q6(w, ql, qh, sc, d)
+        Ws.append((ql, qh, sc, d))
+    del w
+    wbytes = N * K // 2 + N * K // 4 + N * K // 16 + 4 * N * K // 256
+    out = {}
+    for M in Ms:
+        x = torch.from_numpy(gen.activations(gen.STACK36, M, K).view(np.int16)).to(dev)
+        q = torch.empty((M, K), dtype=torch.int8, device=dev)
+        d_a = torch.empty((M, K // 32), dtype=torch.float32, device=dev)
+        y = torch.empty((M, N), dtype=torch.float32, device=dev)
+        reps = 40
+        with torch.cuda.stream(stream):
+            bi.bi_quantize_act_blocks(x, q, d_a)
+            for i in range(2 * copies):
+                bi.bi_linear_q6(q, d_a, *Ws[i % copies], y)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for i in range(reps):
+                bi.bi_linear_q6(q, d_a, *Ws[i % copies], y)
+            e1.record(stream)
+        stream.synchronize()
+        us = e0.elapsed_time(e1) / reps * 1e3
+        gbs = wbytes / (us * 1e-6) / 1e9
+        out[str(M)] = {"us": round(us, 2), "weight_gbs": round(gbs, 1),
+                       "frac_of_hbm_copy": round(gbs / float(peaks["hbm_gbs"]), 4)}
+    out["note"] = ("y fp32 = block-scaled linear, N=24576, K=4096 (%d weight bytes: 6-bit codes, int8 sub-scales "
+                   "per 16, fp32 scales per 256); %d rotating copies > L2" % (wbytes, copies))
+    return out
+
+
 def source_sha(path):
     """Hash of a kernel's source and the headers it is built from."""
     h = hashlib.sha256()
@@ -374,6 +422,11 @@ def run_ours(args):
     setup_s = time.time() - t0
     flags = bi.BI_FLAG_PDL
     stream = torch.cuda.Stream(device=dev)
+    if args.blockq_only:
+        peaks, _ = read_peaks()
+        if rank == 0:
+            print(json.dumps({"block_scaled": blockq_measure(bi, torch, dev, stream, peaks)}), flush=True)
+        return
     if args.prefill_only:
         peaks, _ = read_peaks()
         if rank == 0:
@@ -503,6 +556,7 @@ def run_ours(args):
         traffic = NCU_TRAFFIC["bytes_per_launch"]
 
     prefill = prefill_measure(bi, torch, st, stream, peaks) if not args.no_sweep else None
+    block_scaled = blockq_measure(bi, torch, dev, stream, peaks) if not args.no_sweep else None
     cpu = cpu_baseline(bounded_s=12.0) if rank == 0 else None
     if rank == 0:
         line = {
@@ -537,6 +591,7 @@ def run_ours(args):
             "clocks": clk,
             "cpu_baseline": cpu,
             "prefill": prefill,
+            "block_scaled": block_scaled,
             "setup_s": round(setup_s, 1),
         }
         print(json.dumps(line), flush=True)

@@ -238,6 +238,57 @@ BI_API bi_status bi_greedy_verify(const int32_t *argmax, const int32_t *draft, i
 BI_API bi_status bi_selftest_wait_timeout(void *ws, size_t ws_bytes, bi_stream_t stream);
 
 /*
+ * Block-scaled variant: the mat-vec of "why speculative decoding changed my
+ * output", section "the mat-vec kernel" (q6_k-style weight blocks of 256,
+ * int8 activation blocks of 32, integer products per block, fp32 per-block
+ * scale-and-add in an order fixed for every number of tokens).  The pages
+ * print no storage layout or quantiser; this library's are:
+ *
+ * Weights, K % 256 == 0.  Super-blocks of 256 = 16 sub-blocks of 16; code
+ * c in [-32, 31], int8 sub-scale sc per sub-block, fp32 scale d per
+ * super-block; w ~ c * (d * sc).  Per row n:
+ *   ql [K/2]  low 4 bits of c + 32, element k in byte k/2, bits 4 (k & 1)
+ *   qh [K/4]  high 2 bits of c + 32, element k in byte k/4, bits 2 (k & 3)
+ *   sc [K/16], d [K/256]
+ * Quantiser, per super-block: t_j = absmax_j / 31 (IEEE fp32 division);
+ * d = max_j t_j / 127 (1 if all zero); sc_j = clamp(rne(t_j / d), 0, 127);
+ * e_j = d * sc_j (fp32); c = clamp(rne(w / e_j), -32, 31), 0 where e_j = 0.
+ *   w  fp32 [N, K] (row stride ldw >= K, ldw % 4 == 0), device.
+ *   ql, qh, sc, d  device outputs, row-major as above (16-byte aligned; d 4).
+ * Returns BI_ERR_INVALID_ARG for K not a positive multiple of 256.
+ */
+BI_API bi_status bi_quantize_weight_q6(const float *w, int64_t ldw, int N, int K, uint8_t *ql, uint8_t *qh,
+                                       int8_t *sc, float *d, bi_stream_t stream);
+
+/*
+ * Activation blocks of 32 for the block-scaled linear: the per-token rule of
+ * bi_quantize_act applied to each block of 32 (d_a = absmax / 127, 1 for an
+ * all-zero block; q = clamp(rne(x / d_a), -127, 127), IEEE division).
+ *   x    bf16 [M, K] (row stride ldx >= K), K % 32 == 0
+ *   q    int8 [M, K] out;  d_a  fp32 [M, K/32] out (4-byte aligned)
+ */
+BI_API bi_status bi_quantize_act_blocks(const uint16_t *x, int64_t ldx, int M, int K, int8_t *q, float *d_a,
+                                        bi_stream_t stream);
+
+/*
+ * y = the block-scaled linear, fp32 [M, N] (row stride N), 1 <= M <= 16.
+ * For token m and row n, 32-block b (of K/32) of super-block s = b / 8 holds
+ * sub-blocks j = 2b and 2b + 1:
+ *   isum_b = sc_j * sum(c * q) over its first 16 elements
+ *          + sc_(j+1) * sum over the next 16               (exact integer)
+ *   v_b    = ((float)isum_b * d_a[m][b]) * d[n][s]          (fp32, RNE)
+ * Partial l (l = 0 .. 31) adds v_l, v_(l+32), v_(l+64), ... in that order
+ * starting from +0; then, for offsets 16, 8, 4, 2, 1, every partial becomes
+ * p[l] + p[l xor offset]; y[m][n] = p[0].  The order depends on K only, so
+ * every row is bitwise the same for any M and any other rows in the pass.
+ *   q, d_a  from bi_quantize_act_blocks (q rows 16-byte aligned)
+ *   ql, qh, sc, d  from bi_quantize_weight_q6
+ *   flags   BI_FLAG_PDL or 0
+ */
+BI_API bi_status bi_linear_q6(const int8_t *q, const float *d_a, int M, int K, const uint8_t *ql, const uint8_t *qh,
+                              const int8_t *sc, const float *d, int N, float *y, unsigned flags, bi_stream_t stream);
+
+/*
  * Exhaustive check of the quotient the verify-pass executor quantises with.
  * Codes are clamp(rne(v / s), -127, 127) with v / s an IEEE fp32 division
  * (the per-token absmax quantisation of the W8A8 page, "Quantization").  The

@@ -56,6 +56,12 @@ lib.bi_workspace_status.argtypes = [_vp, _sz, _vp]
 lib.bi_workspace_status.restype = _ci
 lib.bi_linear_w8a8_noalloc.argtypes = [_vp, _vp, _ci, _ci, _vp, _vp, _ci, _vp, _cu, _vp]
 lib.bi_linear_w8a8_noalloc.restype = _ci
+lib.bi_quantize_weight_q6.argtypes = [_vp, _i64, _ci, _ci, _vp, _vp, _vp, _vp, _vp]
+lib.bi_quantize_weight_q6.restype = _ci
+lib.bi_quantize_act_blocks.argtypes = [_vp, _i64, _ci, _ci, _vp, _vp, _vp]
+lib.bi_quantize_act_blocks.restype = _ci
+lib.bi_linear_q6.argtypes = [_vp, _vp, _ci, _ci, _vp, _vp, _vp, _vp, _ci, _vp, _cu, _vp]
+lib.bi_linear_q6.restype = _ci
 
 lib.bi_program_bytes.argtypes = [_ci]
 lib.bi_program_bytes.restype = _sz
@@ -183,6 +189,30 @@ def bi_lmhead_argmax(q: torch.Tensor, s_a: torch.Tensor, w_q: torch.Tensor, s_w:
     _check(lib.bi_lmhead_argmax(_ptr(q), _ptr(s_a), M, K, _ptr(w_q), _ptr(s_w), N, _ptr(logits),
                                 _ptr(argmax), _ptr(ws), ws.numel() * ws.element_size(), flags,
                                 _stream(stream)), "bi_lmhead_argmax")
+
+
+def bi_quantize_weight_q6(w: torch.Tensor, ql: torch.Tensor, qh: torch.Tensor, sc: torch.Tensor, d: torch.Tensor,
+                          stream=None) -> None:
+    """w fp32 [N, K] -> block-scaled ql uint8 [N, K/2], qh uint8 [N, K/4], sc int8 [N, K/16], d fp32 [N, K/256]."""
+    N, K = w.shape
+    _check(lib.bi_quantize_weight_q6(_ptr(w), w.stride(0), N, K, _ptr(ql), _ptr(qh), _ptr(sc), _ptr(d),
+                                     _stream(stream)), "bi_quantize_weight_q6")
+
+
+def bi_quantize_act_blocks(x: torch.Tensor, q: torch.Tensor, d_a: torch.Tensor, stream=None) -> None:
+    """x bf16 bits [M, K] (int16/uint16/bfloat16) -> q int8 [M, K], d_a fp32 [M, K/32]."""
+    M, K = x.shape
+    _check(lib.bi_quantize_act_blocks(_ptr(x), x.stride(0), M, K, _ptr(q), _ptr(d_a), _stream(stream)),
+           "bi_quantize_act_blocks")
+
+
+def bi_linear_q6(q: torch.Tensor, d_a: torch.Tensor, ql: torch.Tensor, qh: torch.Tensor, sc: torch.Tensor,
+                 d: torch.Tensor, y: torch.Tensor, flags: int = 0, stream=None) -> None:
+    """y fp32 [M, N] = the block-scaled linear (1 <= M <= 16)."""
+    M, K = q.shape
+    N = ql.shape[0]
+    _check(lib.bi_linear_q6(_ptr(q), _ptr(d_a), M, K, _ptr(ql), _ptr(qh), _ptr(sc), _ptr(d), N, _ptr(y), flags,
+                            _stream(stream)), "bi_linear_q6")
 
 
 def bi_linear_w8a8_noalloc(q: torch.Tensor, s_a: torch.Tensor, w_q: torch.Tensor, s_w: torch.Tensor,

@@ -308,6 +308,41 @@ bi_status bi_selftest_wait_timeout(void *ws, size_t ws_bytes, bi_stream_t stream
     return from_cuda(bi::launch_wait_selftest(static_cast<int *>(ws), stream));
 }
 
+bi_status bi_quantize_weight_q6(const float *w, int64_t ldw, int N, int K, uint8_t *ql, uint8_t *qh, int8_t *sc,
+                                float *d, bi_stream_t stream)
+{
+    if (!w || !ql || !qh || !sc || !d || N < 1 || K < 256 || (K % 256) != 0 || ldw < K) return BI_ERR_INVALID_ARG;
+    if (!aligned16(w) || (ldw % 4) != 0 || !aligned16(ql) || !aligned16(qh) || !aligned16(sc) || !aligned4(d))
+        return BI_ERR_ALIGNMENT;
+    const bi_status st = device_info(nullptr);
+    if (st != BI_OK) return st;
+    return from_cuda(bi::launch_quantize_q6(w, ldw, N, K, ql, qh, sc, d, stream));
+}
+
+bi_status bi_quantize_act_blocks(const uint16_t *x, int64_t ldx, int M, int K, int8_t *q, float *d_a,
+                                 bi_stream_t stream)
+{
+    if (!x || !q || !d_a || M < 1 || K < 32 || (K % 32) != 0 || ldx < K) return BI_ERR_INVALID_ARG;
+    if (!aligned4(d_a)) return BI_ERR_ALIGNMENT;
+    const bi_status st = device_info(nullptr);
+    if (st != BI_OK) return st;
+    return from_cuda(bi::launch_quantize_act_blocks(x, ldx, M, K, q, d_a, stream));
+}
+
+bi_status bi_linear_q6(const int8_t *q, const float *d_a, int M, int K, const uint8_t *ql, const uint8_t *qh,
+                       const int8_t *sc, const float *d, int N, float *y, unsigned flags, bi_stream_t stream)
+{
+    if (!q || !d_a || !ql || !qh || !sc || !d || !y) return BI_ERR_INVALID_ARG;
+    if (M < 1 || M > 16 || N < 1 || K < 256 || (K % 256) != 0) return BI_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(ql) || !aligned16(qh) || !aligned16(sc) || !aligned4(d) || !aligned4(d_a) ||
+        !aligned4(y))
+        return BI_ERR_ALIGNMENT;
+    const bi_status st = device_info(nullptr);
+    if (st != BI_OK) return st;
+    return from_cuda(
+        bi::launch_linear_q6(q, d_a, M, K, ql, qh, sc, d, N, y, (flags & BI_FLAG_PDL) != 0, stream));
+}
+
 bi_status bi_selftest_quotient(unsigned long long *out, bi_stream_t stream)
 {
     if (!out || (reinterpret_cast<uintptr_t>(out) & 7u) != 0) return BI_ERR_INVALID_ARG;

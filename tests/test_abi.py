@@ -153,3 +153,23 @@ def test_greedy_verify_validation(bi):
     assert V(FAKE, FAKE, 0, FAKE, None) == bi.BI_ERR_INVALID_ARG
     assert V(FAKE + 2, FAKE, 4, FAKE, None) == bi.BI_ERR_ALIGNMENT
     assert V(FAKE, FAKE, 4, FAKE + 1, None) == bi.BI_ERR_ALIGNMENT
+
+
+def test_block_scaled_validation(bi):
+    """The block-scaled entry points: K a multiple of 256 (weights, linear) or
+    32 (activation blocks), 1 <= M <= 16 for the linear, aligned pointers."""
+    W = bi.lib.bi_quantize_weight_q6
+    assert W(FAKE, 1000, 4, 1000, FAKE, FAKE, FAKE, FAKE, None) == bi.BI_ERR_INVALID_ARG      # K % 256
+    assert W(FAKE, 4096, 0, 4096, FAKE, FAKE, FAKE, FAKE, None) == bi.BI_ERR_INVALID_ARG
+    assert W(FAKE, 2048, 4, 4096, FAKE, FAKE, FAKE, FAKE, None) == bi.BI_ERR_INVALID_ARG      # ldw < K
+    assert W(FAKE, 4096, 4, 4096, FAKE + 8, FAKE, FAKE, FAKE, None) == bi.BI_ERR_ALIGNMENT
+    A = bi.lib.bi_quantize_act_blocks
+    assert A(FAKE, 1024, 2, 1000, FAKE, FAKE, None) == bi.BI_ERR_INVALID_ARG                 # K % 32
+    assert A(FAKE, 512, 2, 1024, FAKE, FAKE, None) == bi.BI_ERR_INVALID_ARG                  # ldx < K
+    assert A(None, 1024, 2, 1024, FAKE, FAKE, None) == bi.BI_ERR_INVALID_ARG
+    L = bi.lib.bi_linear_q6
+    assert L(FAKE, FAKE, 17, 4096, FAKE, FAKE, FAKE, FAKE, 8, FAKE, 0, None) == bi.BI_ERR_INVALID_ARG   # M > 16
+    assert L(FAKE, FAKE, 0, 4096, FAKE, FAKE, FAKE, FAKE, 8, FAKE, 0, None) == bi.BI_ERR_INVALID_ARG
+    assert L(FAKE, FAKE, 4, 4000, FAKE, FAKE, FAKE, FAKE, 8, FAKE, 0, None) == bi.BI_ERR_INVALID_ARG    # K % 256
+    assert L(FAKE, FAKE, 4, 4096, FAKE, FAKE, FAKE, FAKE, 8, None, 0, None) == bi.BI_ERR_INVALID_ARG
+    assert L(FAKE + 4, FAKE, 4, 4096, FAKE, FAKE, FAKE, FAKE, 8, FAKE, 0, None) == bi.BI_ERR_ALIGNMENT
