@@ -2,6 +2,7 @@
 // descriptor encoding and kernel dispatch.  Declarations and the contract of
 // every entry point are in include/bi.h.
 #include "bi.h"
+#include "blockq.cuh"
 #include "kernels.cuh"
 #include "ptx.cuh"
 

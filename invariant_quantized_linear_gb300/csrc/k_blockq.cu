@@ -13,6 +13,7 @@
 // Stored layout (per row): ql [K/2] low 4 bits of c + 32 (element k in byte
 // k/2, bits 4 (k & 1)); qh [K/4] high 2 bits (element k in byte k/4, bits
 // 2 (k & 3)); sc [K/16]; d [K/256].
+#include "blockq.cuh"
 #include "kernels.cuh"
 #include "ptx.cuh"
 

@@ -67,14 +67,6 @@ cudaError_t launch_relu_mul_quantize(const uint16_t *gu, int64_t ldgu, int M, in
                                      uint16_t *m_out, bool pdl, cudaStream_t stream);
 cudaError_t launch_wait_selftest(int *status, cudaStream_t stream);
 cudaError_t launch_quotient_selftest(unsigned long long *out, cudaStream_t stream);
-
-// Block-scaled variant (k_blockq.cu).
-cudaError_t launch_quantize_q6(const float *w, int64_t ldw, int N, int K, uint8_t *ql, uint8_t *qh, int8_t *sc,
-                               float *d, cudaStream_t stream);
-cudaError_t launch_quantize_act_blocks(const uint16_t *x, int64_t ldx, int M, int K, int8_t *q, float *d_a,
-                                       cudaStream_t stream);
-cudaError_t launch_linear_q6(const int8_t *qa, const float *d_a, int M, int K, const uint8_t *ql, const uint8_t *qh,
-                             const int8_t *sc, const float *d, int N, float *y, bool pdl, cudaStream_t stream);
 cudaError_t launch_greedy_verify(const int32_t *argmax, const int32_t *draft, int M, int32_t *out,
                                  cudaStream_t stream);
 cudaError_t launch_quantize_weight(const float *w, int64_t ldw, int N, int K, int8_t *w_q, float *s_w,
