@@ -52,6 +52,10 @@ def lib():
         L.oracle_quantize_act_blocks.restype = None
         L.oracle_linear_q6.argtypes = [vp, vp, ci, ci, vp, vp, vp, vp, ci, vp]
         L.oracle_linear_q6.restype = None
+        L.oracle_attn_exp.argtypes = [ctypes.c_float]
+        L.oracle_attn_exp.restype = ctypes.c_float
+        L.oracle_attention.argtypes = [vp, vp, vp, ci, ci, ci, ci, ci, ctypes.c_float, vp]
+        L.oracle_attention.restype = None
         L.oracle_num_threads.argtypes = []
         L.oracle_num_threads.restype = ci
         _LIB = L
@@ -266,6 +270,27 @@ def linear_q6(qa, d_a, ql, qh, sc, d) -> np.ndarray:
     lib().oracle_linear_q6(qa.ctypes.data, d_a.ctypes.data, M, K, ql.ctypes.data, qh.ctypes.data, sc.ctypes.data,
                            d.ctypes.data, N, y.ctypes.data)
     return y
+
+
+# ------------------------------------------------------------ split-KV attention
+# ("My speculative decoder got slower", split-KV attention; "why speculative
+# decoding changed my output", "attention"; the readings are in oracle.c)
+
+def attn_exp(x: float) -> float:
+    """The attention's exp e(x) for x <= 0, as defined in oracle.c."""
+    return float(lib().oracle_attn_exp(x))
+
+
+def attention(q, k, v, T0: int, scale: float) -> np.ndarray:
+    """q bf16 [M, Hq, D], k / v bf16 [S, Hkv, D] (S >= T0 + M) -> o bf16 [M, Hq, D]:
+    query m attends to positions 0 .. T0 + m, in 256-position chunks merged in order."""
+    q, k, v = _c(q, np.uint16), _c(k, np.uint16), _c(v, np.uint16)
+    M, Hq, D = q.shape
+    Hkv = k.shape[1]
+    assert k.shape[0] >= T0 + M and Hq % Hkv == 0
+    o = np.empty((M, Hq, D), np.uint16)
+    lib().oracle_attention(q.ctypes.data, k.ctypes.data, v.ctypes.data, M, Hq, Hkv, D, T0, scale, o.ctypes.data)
+    return o
 
 
 def num_threads() -> int:

@@ -467,6 +467,124 @@ void oracle_linear_q6(const int8_t *qa, const float *d_a, int M, int K, const ui
         }
 }
 
+/* ------------------------------------------------ split-KV attention
+ *
+ * The verify pass's attention, batch-invariant: "My speculative decoder got
+ * slower" (the split-KV attention: the cache cut into 256-token chunks, one
+ * partial result per chunk, then a merge; one chunk writes the output
+ * directly) and "why speculative decoding changed my output" (section
+ * "attention": a batch of queries must use the one-query geometry).
+ *
+ * Readings used on both sides:
+ *  - query m (of M) attends to cache positions 0 .. T0 + m (causal);
+ *    head h uses kv head h / (Hq / Hkv); s_t = (sum over d in order of
+ *    q_d * k_td, fp32, from +0) * scale;
+ *  - chunk c holds positions 256 c .. 256 c + 255 of those; per chunk:
+ *    mx = max s_t; p_t = e(s_t - mx); l = sum of p_t in position order;
+ *    a_d = sum of p_t * v_td in position order (fp32, from +0);
+ *  - merge over chunks in order: mx* = max mx_c; w_c = e(mx_c - mx*);
+ *    L = sum w_c * l_c; o_d = (sum w_c * a_cd) / L; o is rounded to bf16.
+ *    With one chunk w_0 = e(0) = 1 and the merge changes nothing.
+ *  - e(x), x <= 0: t = x * log2(e); 0 if t < -126; else n = rne(t),
+ *    f = t - n (exact, |f| <= 1/2), 2^f by the Taylor polynomial of
+ *    e^(f ln 2) to degree 6, times 2^n (one rounding).  ln 2 and log2(e) are
+ *    their fp32 roundings (0x3F317218, 0x3FB8AA3B); the coefficients come
+ *    from the recurrence c_0 = 1, c_k = (c_(k-1) * ln 2) / k in fp32; the
+ *    polynomial is evaluated by Horner, one multiply then one add per step.
+ * The chunk count follows the positions a query sees, never the allocated
+ * cache size.
+ */
+static const float kLn2 = 0.693147182464599609375f;    /* ln 2 rounded to fp32 (0x3F317218) */
+static const float kLog2e = 1.44269502162933349609375f; /* log2(e) rounded to fp32 (0x3FB8AA3B) */
+
+static float e_f32(float x)
+{
+    float c[7];
+    c[0] = 1.0f;
+    for (int k = 1; k < 7; ++k) {
+        float u = c[k - 1] * kLn2;
+        c[k] = u / (float)k;
+    }
+    float t = x * kLog2e;
+    if (t < -126.0f) return 0.0f;
+    float n = rne_f((double)t);
+    float f = t - n;
+    float p = c[6];
+    for (int k = 5; k >= 0; --k) {
+        p = p * f;
+        p = p + c[k];
+    }
+    return ldexpf(p, (int)n);
+}
+
+float oracle_attn_exp(float x) { return e_f32(x); }
+
+void oracle_attention(const uint16_t *q, const uint16_t *kc, const uint16_t *vc, int M, int Hq, int Hkv, int D,
+                      int T0, float scale, uint16_t *o)
+{
+    const int g = Hq / Hkv;
+#pragma omp parallel for schedule(static) collapse(2)
+    for (int m = 0; m < M; ++m)
+        for (int h = 0; h < Hq; ++h) {
+            const int hk = h / g, T = T0 + m + 1;      /* positions 0 .. T0 + m */
+            const int C = (T + 255) / 256;
+            float *mxc = (float *)malloc(sizeof(float) * C), *lc = (float *)malloc(sizeof(float) * C);
+            float *ac = (float *)malloc(sizeof(float) * (size_t)C * D);
+            float *s = (float *)malloc(sizeof(float) * 256);
+            const uint16_t *qr = q + ((int64_t)m * Hq + h) * D;
+            for (int c = 0; c < C; ++c) {
+                const int t0 = 256 * c, t1 = (t0 + 256 < T) ? t0 + 256 : T;
+                float mx = -INFINITY;
+                for (int t = t0; t < t1; ++t) {
+                    const uint16_t *kr = kc + ((int64_t)t * Hkv + hk) * D;
+                    float acc = 0.0f;
+                    for (int d = 0; d < D; ++d) {
+                        float prod = oracle_bf16_to_f32(qr[d]) * oracle_bf16_to_f32(kr[d]);
+                        acc = acc + prod;
+                    }
+                    s[t - t0] = acc * scale;
+                    if (s[t - t0] > mx) mx = s[t - t0];
+                }
+                float l = 0.0f;
+                float *a = ac + (size_t)c * D;
+                for (int d = 0; d < D; ++d) a[d] = 0.0f;
+                for (int t = t0; t < t1; ++t) {
+                    const float p = e_f32(s[t - t0] - mx);
+                    l = l + p;
+                    const uint16_t *vr = vc + ((int64_t)t * Hkv + hk) * D;
+                    for (int d = 0; d < D; ++d) {
+                        float prod = p * oracle_bf16_to_f32(vr[d]);
+                        a[d] = a[d] + prod;
+                    }
+                }
+                mxc[c] = mx;
+                lc[c] = l;
+            }
+            float mx = mxc[0];
+            for (int c = 1; c < C; ++c)
+                if (mxc[c] > mx) mx = mxc[c];
+            float L = 0.0f;
+            for (int c = 0; c < C; ++c) {
+                float w = e_f32(mxc[c] - mx);
+                float wl = w * lc[c];
+                L = L + wl;
+            }
+            for (int d = 0; d < D; ++d) {
+                float num = 0.0f;
+                for (int c = 0; c < C; ++c) {
+                    float w = e_f32(mxc[c] - mx);
+                    float wa = w * ac[(size_t)c * D + d];
+                    num = num + wa;
+                }
+                o[((int64_t)m * Hq + h) * D + d] = oracle_f32_to_bf16_rne(num / L);
+            }
+            free(mxc);
+            free(lc);
+            free(ac);
+            free(s);
+        }
+}
+
 /* Number of OpenMP threads the parallel loops above use (1 without OpenMP). */
 int oracle_num_threads(void)
 {
