@@ -31,6 +31,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -69,6 +70,8 @@ def parse():
                    help="time only the prefill contraction at M tokens and print its figures")
     p.add_argument("--blockq-only", action="store_true",
                    help="time only the block-scaled variant and print its figures")
+    p.add_argument("--attn-only", action="store_true",
+                   help="time only the split-KV verify attention and print its figures")
     p.add_argument("--mode", default="program", choices=["program", "calls"],
                    help="program: the step as one verify-pass program launch; calls: one launch per op")
     return p.parse_args()
@@ -395,6 +398,56 @@ def blockq_measure(bi, torch, dev, stream, peaks, Ms=(1, 8, 16)):
     return out
 
 
+def attention_measure(bi, torch, dev, stream, peaks, cases=((8, 4096, 36), (8, 32768, 4), (1, 4096, 36))):
+    """The split-KV verify attention of a Qwen3-8B-shaped layer (32 query heads
+    over 8 kv heads of 128) through bi_attention_verify, timed alone, for
+    (M queries, T0 cached positions, cache copies): the copies (one per layer
+    of a verify pass) rotate so that each call reads its cache from HBM.
+    Reported: microseconds per call, cache bytes read per second, and the
+    fp32 operations of the fixed-order arithmetic (a multiply and an add per
+    element for the scores and again for the weighted values) per second
+    against the fp32 issue rate of the SMs (152 SMs x 128 lanes x the clock)."""
+    import gen
+    Hq, Hkv, D = 32, 8, 128
+    scale = 1.0 / math.sqrt(D)
+    sm_ops = 152 * 128 * 2.07e9
+    out = {}
+    for M, T0, copies in cases:
+        S = T0 + M
+        q, k, v = gen.attn_qkv(gen.ATTENTION_SEED, M, Hq, Hkv, D, S)
+        q_t = torch.from_numpy(q.view(np.int16)).to(dev)
+        k0 = torch.from_numpy(k.view(np.int16)).to(dev)
+        v0 = torch.from_numpy(v.view(np.int16)).to(dev)
+        caches = [(k0.clone(), v0.clone()) for _ in range(copies)]
+        del k0, v0
+        o = torch.empty((M, Hq, D), dtype=torch.int16, device=dev)
+        n = bi.bi_attention_workspace_size(M, Hq, D, T0)
+        ws = torch.empty(max(n, 16), dtype=torch.uint8, device=dev)
+        reps = max(2 * copies, 40)
+        with torch.cuda.stream(stream):
+            for i in range(2 * copies):
+                bi.bi_attention_verify(q_t, *caches[i % copies], T0, scale, o, ws)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for i in range(reps):
+                bi.bi_attention_verify(q_t, *caches[i % copies], T0, scale, o, ws)
+            e1.record(stream)
+        stream.synchronize()
+        us = e0.elapsed_time(e1) / reps * 1e3
+        kv_bytes = 2 * S * Hkv * D * 2
+        ops = 4 * D * Hq * sum(T0 + m + 1 for m in range(M))
+        out["M%d_T%d" % (M, T0)] = {
+            "us": round(us, 2), "kv_gbs": round(kv_bytes / (us * 1e-6) / 1e9, 1),
+            "frac_of_hbm_copy": round(kv_bytes / (us * 1e-6) / 1e9 / float(peaks["hbm_gbs"]), 4),
+            "fp32_tops": round(ops / (us * 1e-6) / 1e12, 2), "frac_of_fp32_issue": round(ops / (us * 1e-6) / sm_ops, 4),
+            "kv_bytes": kv_bytes, "copies": copies}
+        del caches
+    out["note"] = ("Hq=32, Hkv=8, D=128, bf16 q/k/v ~ N(0,1); query m sees positions 0..T0+m; 256-position chunks "
+                   "merged in order; rotating cache copies > L2")
+    return out
+
+
 def source_sha(path):
     """Hash of a kernel's source and the headers it is built from."""
     h = hashlib.sha256()
@@ -417,6 +470,12 @@ def run_ours(args):
 
     M = args.m
     assert 1 <= M <= 16
+    if args.attn_only:
+        peaks, _ = read_peaks()
+        if rank == 0:
+            stream = torch.cuda.Stream(device=dev)
+            print(json.dumps({"attention": attention_measure(bi, torch, dev, stream, peaks)}), flush=True)
+        return
     t0 = time.time()
     st = Stack(bi, torch, args.layers, dev)
     setup_s = time.time() - t0
@@ -557,6 +616,7 @@ def run_ours(args):
 
     prefill = prefill_measure(bi, torch, st, stream, peaks) if not args.no_sweep else None
     block_scaled = blockq_measure(bi, torch, dev, stream, peaks) if not args.no_sweep else None
+    attention = attention_measure(bi, torch, dev, stream, peaks) if not args.no_sweep else None
     cpu = cpu_baseline(bounded_s=12.0) if rank == 0 else None
     if rank == 0:
         line = {
@@ -592,6 +652,7 @@ def run_ours(args):
             "cpu_baseline": cpu,
             "prefill": prefill,
             "block_scaled": block_scaled,
+            "attention": attention,
             "setup_s": round(setup_s, 1),
         }
         print(json.dumps(line), flush=True)

@@ -16,6 +16,9 @@ Workloads (shapes and seeds; every one synthetic, no checkpoint or dataset):
 * ``stack36``    - all linears of a 36-layer Qwen3-8B-shaped stack plus the
   LM head, power-of-two scales, seed 3, M in {1,5}.
 * ``prefill``    - M in {512, 2048}, K=4096, N=12288, seed 4.
+* ``attention``  - verify-pass attention of a Qwen3-8B-shaped layer: 32 query
+  heads over 8 kv heads of 128, M = 8 queries after T0 = 4096 cached
+  positions, seed 5; q, k, v ~ N(0, 1) as bf16 (``attn_qkv``).
 
 Weights are ~N(0, 0.02) and activations ~N(0, 1) (Irwin-Hall(8) approximation,
 see gen.c); ``single``, ``qwen3_8b`` and ``prefill`` activations carry four
@@ -97,6 +100,19 @@ def act_bf16(seed: int, stream: int, rows: int, cols: int, sigma: float = 1.0,
     lib().gen_act_bf16(seed, stream, row0, rows, cols, ld, sigma,
                        _ptr(o) if o.size else None, int(o.size), gain, _ptr(out))
     return out
+
+
+ATTENTION_SEED = 5
+
+
+def attn_qkv(seed: int, M: int, Hq: int, Hkv: int, D: int, S: int, sigma_q: float = 1.0,
+             sigma_k: float = 1.0) -> tuple:
+    """bf16 bit patterns of q [M, Hq, D] (stream 20), k [S, Hkv, D] (stream 21,
+    standard deviation sigma_k) and v [S, Hkv, D] (stream 22, N(0, 1))."""
+    q = act_bf16(seed, 20, M, Hq * D, sigma_q).reshape(M, Hq, D)
+    k = act_bf16(seed, 21, S, Hkv * D, sigma_k).reshape(S, Hkv, D)
+    v = act_bf16(seed, 22, S, Hkv * D, 1.0).reshape(S, Hkv, D)
+    return q, k, v
 
 
 def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:

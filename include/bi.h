@@ -289,6 +289,37 @@ BI_API bi_status bi_linear_q6(const int8_t *q, const float *d_a, int M, int K, c
                               const int8_t *sc, const float *d, int N, float *y, unsigned flags, bi_stream_t stream);
 
 /*
+ * Split-KV attention of a verify pass, batch-invariant ("My speculative
+ * decoder got slower", split-KV attention in 256-token chunks with a merge;
+ * "why speculative decoding changed my output", "attention").  Query m
+ * (0 .. M-1) attends to cache positions 0 .. T0 + m; query head h reads kv
+ * head h / (Hq / Hkv).  Per query, head and chunk c (positions 256c ..
+ * 256c + 255 of those), fp32, every operation rounded once:
+ *   s_t = (sum over d in order of q_d k_td, from +0) * scale
+ *   mx  = max s_t,  p_t = e(s_t - mx),  l = sum of p_t in position order,
+ *   a_d = sum of p_t v_td in position order;
+ * then over the query's chunks in order: mx* = max mx_c, w_c = e(mx_c - mx*),
+ * L = sum w_c l_c, o_d = bf16_rne((sum w_c a_cd) / L).  e(x) for x <= 0:
+ * t = x log2(e) (fp32 constant 0x3FB8AA3B); 0 if t < -126; else n = rne(t),
+ * f = t - n, 2^f by the degree-6 Taylor polynomial of e^(f ln 2) in Horner
+ * form with c_0 = 1, c_k = (c_(k-1) ln 2) / k (ln 2 = 0x3F317218), times 2^n.
+ * A query's result depends only on its own positions: the same bits for any
+ * M, any T0 that leaves it the same cache, and alone or in a batch.
+ *   q      bf16 [M, Hq, D]          k, v  bf16 [S, Hkv, D] (k 16-byte aligned)
+ *   o      bf16 [M, Hq, D] out      D = 64 or 128; Hq % Hkv == 0; T0 + M <= S
+ *   ws     device workspace of at least bi_attention_workspace_size(M, Hq,
+ *          D, T0) bytes, 4-byte aligned (null when that size is 0); its
+ *          contents need no initialisation and are overwritten.
+ * One or two launches on `stream` (the second merges when the last query
+ * covers more than one chunk).  Returns BI_ERR_INVALID_ARG for a null
+ * pointer or an out-of-range size, BI_ERR_ALIGNMENT, BI_ERR_WORKSPACE.
+ */
+BI_API size_t bi_attention_workspace_size(int M, int Hq, int D, int T0);
+BI_API bi_status bi_attention_verify(const uint16_t *q, const uint16_t *k, const uint16_t *v, int M, int Hq, int Hkv,
+                                     int D, int T0, int S, float scale, uint16_t *o, void *ws, size_t ws_bytes,
+                                     bi_stream_t stream);
+
+/*
  * Exhaustive check of the quotient the verify-pass executor quantises with.
  * Codes are clamp(rne(v / s), -127, 127) with v / s an IEEE fp32 division
  * (the per-token absmax quantisation of the W8A8 page, "Quantization").  The

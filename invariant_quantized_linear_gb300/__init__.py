@@ -62,6 +62,11 @@ lib.bi_quantize_act_blocks.argtypes = [_vp, _i64, _ci, _ci, _vp, _vp, _vp]
 lib.bi_quantize_act_blocks.restype = _ci
 lib.bi_linear_q6.argtypes = [_vp, _vp, _ci, _ci, _vp, _vp, _vp, _vp, _ci, _vp, _cu, _vp]
 lib.bi_linear_q6.restype = _ci
+lib.bi_attention_workspace_size.argtypes = [_ci, _ci, _ci, _ci]
+lib.bi_attention_workspace_size.restype = _sz
+lib.bi_attention_verify.argtypes = [_vp, _vp, _vp, _ci, _ci, _ci, _ci, _ci, _ci, ctypes.c_float, _vp, _vp, _sz,
+                                    _vp]
+lib.bi_attention_verify.restype = _ci
 
 lib.bi_program_bytes.argtypes = [_ci]
 lib.bi_program_bytes.restype = _sz
@@ -213,6 +218,23 @@ def bi_linear_q6(q: torch.Tensor, d_a: torch.Tensor, ql: torch.Tensor, qh: torch
     N = ql.shape[0]
     _check(lib.bi_linear_q6(_ptr(q), _ptr(d_a), M, K, _ptr(ql), _ptr(qh), _ptr(sc), _ptr(d), N, _ptr(y), flags,
                             _stream(stream)), "bi_linear_q6")
+
+
+def bi_attention_workspace_size(M: int, Hq: int, D: int, T0: int) -> int:
+    return int(lib.bi_attention_workspace_size(M, Hq, D, T0))
+
+
+def bi_attention_verify(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, T0: int, scale: float, o: torch.Tensor,
+                        ws: torch.Tensor | None = None, stream=None) -> None:
+    """Split-KV verify attention: q bf16 [M, Hq, D], k/v bf16 [S, Hkv, D]
+    (contiguous), o bf16 [M, Hq, D] out; query m sees positions 0 .. T0 + m.
+    ws: device buffer of at least bi_attention_workspace_size(M, Hq, D, T0)
+    bytes, or None when that is 0."""
+    M, Hq, D = q.shape
+    S, Hkv = k.shape[0], k.shape[1]
+    nbytes = 0 if ws is None else ws.numel() * ws.element_size()
+    _check(lib.bi_attention_verify(_ptr(q), _ptr(k), _ptr(v), M, Hq, Hkv, D, T0, S, scale, _ptr(o), _ptr(ws),
+                                   nbytes, _stream(stream)), "bi_attention_verify")
 
 
 def bi_linear_w8a8_noalloc(q: torch.Tensor, s_a: torch.Tensor, w_q: torch.Tensor, s_w: torch.Tensor,

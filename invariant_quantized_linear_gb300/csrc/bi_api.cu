@@ -1,6 +1,7 @@
 // C ABI of the batch-invariant W8A8 library: argument validation, TMA
 // descriptor encoding and kernel dispatch.  Declarations and the contract of
 // every entry point are in include/bi.h.
+#include "attn.cuh"
 #include "bi.h"
 #include "blockq.cuh"
 #include "kernels.cuh"
@@ -16,6 +17,7 @@ namespace {
 using bi::kMaxGrid;
 
 constexpr long long kMaxK = 133144;  // largest K with K * 127^2 < 2^31
+constexpr int kMaxAttnQueries = 4096; // queries of one attention call (grid z)
 
 bool aligned16(const void *p)
 {
@@ -342,6 +344,47 @@ bi_status bi_linear_q6(const int8_t *q, const float *d_a, int M, int K, const ui
     if (st != BI_OK) return st;
     return from_cuda(
         bi::launch_linear_q6(q, d_a, M, K, ql, qh, sc, d, N, y, (flags & BI_FLAG_PDL) != 0, stream));
+}
+
+size_t bi_attention_workspace_size(int M, int Hq, int D, int T0)
+{
+    if (M < 1 || M > kMaxAttnQueries || Hq < 1 || Hq > 65535 || (D != 64 && D != 128) || T0 < 0 ||
+        T0 > INT32_MAX - M)
+        return 0;
+    const int C = bi::attn_chunks(T0, M);
+    if (C == 1) return 0;
+    return static_cast<size_t>(M) * Hq * C * (D + 2) * sizeof(float);
+}
+
+bi_status bi_attention_verify(const uint16_t *q, const uint16_t *k, const uint16_t *v, int M, int Hq, int Hkv, int D,
+                              int T0, int S, float scale, uint16_t *o, void *ws, size_t ws_bytes, bi_stream_t stream)
+{
+    if (!q || !k || !v || !o) return BI_ERR_INVALID_ARG;
+    if (M < 1 || M > kMaxAttnQueries || Hq < 1 || Hq > 65535 || Hkv < 1 || (Hq % Hkv) != 0 ||
+        (D != 64 && D != 128) || T0 < 0 || S < 1 || T0 > S - M || !(scale == scale) || scale == INFINITY ||
+        scale == -INFINITY)
+        return BI_ERR_INVALID_ARG;
+    if (!aligned16(k) || (reinterpret_cast<uintptr_t>(q) & 1u) || (reinterpret_cast<uintptr_t>(v) & 1u) ||
+        (reinterpret_cast<uintptr_t>(o) & 1u))
+        return BI_ERR_ALIGNMENT;
+    const size_t need = bi_attention_workspace_size(M, Hq, D, T0);
+    if (need > 0 && (!ws || ws_bytes < need || !aligned4(ws))) return BI_ERR_WORKSPACE;
+    const bi_status st = device_info(nullptr);
+    if (st != BI_OK) return st;
+    bi::AttnArgs a;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.o = o;
+    a.ws = static_cast<float *>(ws);
+    a.scale = scale;
+    a.M = M;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.D = D;
+    a.T0 = T0;
+    a.Cmax = bi::attn_chunks(T0, M);
+    return from_cuda(bi::launch_attention(a, stream));
 }
 
 bi_status bi_selftest_quotient(unsigned long long *out, bi_stream_t stream)

@@ -173,3 +173,35 @@ def test_block_scaled_validation(bi):
     assert L(FAKE, FAKE, 4, 4000, FAKE, FAKE, FAKE, FAKE, 8, FAKE, 0, None) == bi.BI_ERR_INVALID_ARG    # K % 256
     assert L(FAKE, FAKE, 4, 4096, FAKE, FAKE, FAKE, FAKE, 8, None, 0, None) == bi.BI_ERR_INVALID_ARG
     assert L(FAKE + 4, FAKE, 4, 4096, FAKE, FAKE, FAKE, FAKE, 8, FAKE, 0, None) == bi.BI_ERR_ALIGNMENT
+
+
+def test_attention_validation(bi):
+    """The split-KV attention: D of 64 or 128, Hq a multiple of Hkv, the last
+    query's positions inside the cache, a finite scale, k 16-byte aligned and a
+    workspace once a query covers more than one chunk of 256 positions."""
+    Z = bi.lib.bi_attention_workspace_size
+    assert Z(8, 32, 128, 100) == 0                       # 108 positions: one chunk
+    assert Z(8, 32, 128, 1000) == 8 * 32 * 4 * 130 * 4   # 1008 positions: 4 chunks
+    assert Z(1, 1, 64, 256) == 2 * 66 * 4
+    assert Z(8, 32, 96, 1000) == 0 and Z(0, 32, 128, 1000) == 0
+    F = bi.lib.bi_attention_verify
+    args = dict(q=FAKE, k=FAKE, v=FAKE, M=8, Hq=32, Hkv=8, D=128, T0=1000, S=1008, scale=0.088, o=FAKE, ws=None,
+                ws_bytes=0, stream=None)
+
+    def call(**kw):
+        a = dict(args, **kw)
+        return F(a["q"], a["k"], a["v"], a["M"], a["Hq"], a["Hkv"], a["D"], a["T0"], a["S"], a["scale"], a["o"],
+                 a["ws"], a["ws_bytes"], a["stream"])
+
+    assert call(D=96) == bi.BI_ERR_INVALID_ARG
+    assert call(Hkv=5) == bi.BI_ERR_INVALID_ARG
+    assert call(S=1007) == bi.BI_ERR_INVALID_ARG          # T0 + M > S
+    assert call(M=0) == bi.BI_ERR_INVALID_ARG
+    assert call(T0=-1) == bi.BI_ERR_INVALID_ARG
+    assert call(scale=float("nan")) == bi.BI_ERR_INVALID_ARG
+    assert call(scale=float("inf")) == bi.BI_ERR_INVALID_ARG
+    assert call(o=None) == bi.BI_ERR_INVALID_ARG
+    assert call(k=FAKE + 2) == bi.BI_ERR_ALIGNMENT
+    assert call(v=FAKE + 1) == bi.BI_ERR_ALIGNMENT
+    assert call() == bi.BI_ERR_WORKSPACE                  # 4 chunks, no workspace
+    assert call(ws=FAKE, ws_bytes=Z(8, 32, 128, 1000) - 1) == bi.BI_ERR_WORKSPACE
