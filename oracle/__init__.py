@@ -56,6 +56,10 @@ def lib():
         L.oracle_attn_exp.restype = ctypes.c_float
         L.oracle_attention.argtypes = [vp, vp, vp, ci, ci, ci, ci, ci, ctypes.c_float, vp]
         L.oracle_attention.restype = None
+        L.oracle_attention_chunk.argtypes = [vp, vp, vp, ci, ci, ci, ci, ci, ctypes.c_float, vp, vp, vp]
+        L.oracle_attention_chunk.restype = None
+        L.oracle_attention_merge.argtypes = [ci, vp, vp, vp, ci, vp]
+        L.oracle_attention_merge.restype = None
         L.oracle_num_threads.argtypes = []
         L.oracle_num_threads.restype = ci
         _LIB = L
@@ -290,6 +294,28 @@ def attention(q, k, v, T0: int, scale: float) -> np.ndarray:
     assert k.shape[0] >= T0 + M and Hq % Hkv == 0
     o = np.empty((M, Hq, D), np.uint16)
     lib().oracle_attention(q.ctypes.data, k.ctypes.data, v.ctypes.data, M, Hq, Hkv, D, T0, scale, o.ctypes.data)
+    return o
+
+
+def attention_chunk(q_row, k, v, hk: int, t0: int, t1: int, scale: float):
+    """One chunk (positions t0 .. t1 - 1, at most 256) of kv head hk for one
+    query row q_row bf16 [D]: (mx, l, a fp32 [D])."""
+    q_row, k, v = _c(q_row, np.uint16), _c(k, np.uint16), _c(v, np.uint16)
+    D = q_row.shape[0]
+    assert 0 <= t0 < t1 <= k.shape[0] and t1 - t0 <= 256
+    mx, l = np.zeros(1, np.float32), np.zeros(1, np.float32)
+    a = np.empty(D, np.float32)
+    lib().oracle_attention_chunk(q_row.ctypes.data, k.ctypes.data, v.ctypes.data, k.shape[1], hk, D, t0, t1, scale,
+                                 mx.ctypes.data, l.ctypes.data, a.ctypes.data)
+    return mx[0], l[0], a
+
+
+def attention_merge(mx, l, a) -> np.ndarray:
+    """The in-order merge of C chunk results: mx [C], l [C], a [C, D] (fp32) -> o bf16 [D]."""
+    mx, l, a = _c(mx, np.float32), _c(l, np.float32), _c(a, np.float32)
+    C, D = a.shape
+    o = np.empty(D, np.uint16)
+    lib().oracle_attention_merge(C, mx.ctypes.data, l.ctypes.data, a.ctypes.data, D, o.ctypes.data)
     return o
 
 

@@ -476,6 +476,8 @@ void oracle_linear_q6(const int8_t *qa, const float *d_a, int M, int K, const ui
  * "attention": a batch of queries must use the one-query geometry).
  *
  * Readings used on both sides:
+ *  - every step acc <- acc + x * y below is one fused multiply-add
+ *    (fmaf: one rounding); every other operation is one fp32 operation;
  *  - query m (of M) attends to cache positions 0 .. T0 + m (causal);
  *    head h uses kv head h / (Hq / Hkv); s_t = (sum over d in order of
  *    q_d * k_td, fp32, from +0) * scale;
@@ -490,7 +492,7 @@ void oracle_linear_q6(const int8_t *qa, const float *d_a, int M, int K, const ui
  *    e^(f ln 2) to degree 6, times 2^n (one rounding).  ln 2 and log2(e) are
  *    their fp32 roundings (0x3F317218, 0x3FB8AA3B); the coefficients come
  *    from the recurrence c_0 = 1, c_k = (c_(k-1) * ln 2) / k in fp32; the
- *    polynomial is evaluated by Horner, one multiply then one add per step.
+ *    polynomial is evaluated by Horner, p <- p * f + c_k (fused) per step.
  * The chunk count follows the positions a query sees, never the allocated
  * cache size.
  */
@@ -510,14 +512,52 @@ static float e_f32(float x)
     float n = rne_f((double)t);
     float f = t - n;
     float p = c[6];
-    for (int k = 5; k >= 0; --k) {
-        p = p * f;
-        p = p + c[k];
-    }
+    for (int k = 5; k >= 0; --k) p = fmaf(p, f, c[k]);
     return ldexpf(p, (int)n);
 }
 
 float oracle_attn_exp(float x) { return e_f32(x); }
+
+/* One chunk: positions t0 .. t1 - 1 (t1 - t0 <= 256) of kv head hk for the
+ * query row qr [D]: its maximum score mx, weight sum l and weighted values a [D]. */
+void oracle_attention_chunk(const uint16_t *qr, const uint16_t *kc, const uint16_t *vc, int Hkv, int hk, int D,
+                            int t0, int t1, float scale, float *mx_out, float *l_out, float *a)
+{
+    float s[256];
+    float mx = -INFINITY;
+    for (int t = t0; t < t1; ++t) {
+        const uint16_t *kr = kc + ((int64_t)t * Hkv + hk) * D;
+        float acc = 0.0f;
+        for (int d = 0; d < D; ++d) acc = fmaf(oracle_bf16_to_f32(qr[d]), oracle_bf16_to_f32(kr[d]), acc);
+        s[t - t0] = acc * scale;
+        if (s[t - t0] > mx) mx = s[t - t0];
+    }
+    float l = 0.0f;
+    for (int d = 0; d < D; ++d) a[d] = 0.0f;
+    for (int t = t0; t < t1; ++t) {
+        const float p = e_f32(s[t - t0] - mx);
+        l = l + p;
+        const uint16_t *vr = vc + ((int64_t)t * Hkv + hk) * D;
+        for (int d = 0; d < D; ++d) a[d] = fmaf(p, oracle_bf16_to_f32(vr[d]), a[d]);
+    }
+    *mx_out = mx;
+    *l_out = l;
+}
+
+/* The merge of C chunk results (mxc [C], lc [C], ac [C][D]) into o [D] (bf16). */
+void oracle_attention_merge(int C, const float *mxc, const float *lc, const float *ac, int D, uint16_t *o)
+{
+    float mx = mxc[0];
+    for (int c = 1; c < C; ++c)
+        if (mxc[c] > mx) mx = mxc[c];
+    float L = 0.0f;
+    for (int c = 0; c < C; ++c) L = fmaf(e_f32(mxc[c] - mx), lc[c], L);
+    for (int d = 0; d < D; ++d) {
+        float num = 0.0f;
+        for (int c = 0; c < C; ++c) num = fmaf(e_f32(mxc[c] - mx), ac[(size_t)c * D + d], num);
+        o[d] = oracle_f32_to_bf16_rne(num / L);
+    }
+}
 
 void oracle_attention(const uint16_t *q, const uint16_t *kc, const uint16_t *vc, int M, int Hq, int Hkv, int D,
                       int T0, float scale, uint16_t *o)
@@ -526,62 +566,19 @@ void oracle_attention(const uint16_t *q, const uint16_t *kc, const uint16_t *vc,
 #pragma omp parallel for schedule(static) collapse(2)
     for (int m = 0; m < M; ++m)
         for (int h = 0; h < Hq; ++h) {
-            const int hk = h / g, T = T0 + m + 1;      /* positions 0 .. T0 + m */
+            const int T = T0 + m + 1;                  /* positions 0 .. T0 + m */
             const int C = (T + 255) / 256;
             float *mxc = (float *)malloc(sizeof(float) * C), *lc = (float *)malloc(sizeof(float) * C);
             float *ac = (float *)malloc(sizeof(float) * (size_t)C * D);
-            float *s = (float *)malloc(sizeof(float) * 256);
-            const uint16_t *qr = q + ((int64_t)m * Hq + h) * D;
             for (int c = 0; c < C; ++c) {
                 const int t0 = 256 * c, t1 = (t0 + 256 < T) ? t0 + 256 : T;
-                float mx = -INFINITY;
-                for (int t = t0; t < t1; ++t) {
-                    const uint16_t *kr = kc + ((int64_t)t * Hkv + hk) * D;
-                    float acc = 0.0f;
-                    for (int d = 0; d < D; ++d) {
-                        float prod = oracle_bf16_to_f32(qr[d]) * oracle_bf16_to_f32(kr[d]);
-                        acc = acc + prod;
-                    }
-                    s[t - t0] = acc * scale;
-                    if (s[t - t0] > mx) mx = s[t - t0];
-                }
-                float l = 0.0f;
-                float *a = ac + (size_t)c * D;
-                for (int d = 0; d < D; ++d) a[d] = 0.0f;
-                for (int t = t0; t < t1; ++t) {
-                    const float p = e_f32(s[t - t0] - mx);
-                    l = l + p;
-                    const uint16_t *vr = vc + ((int64_t)t * Hkv + hk) * D;
-                    for (int d = 0; d < D; ++d) {
-                        float prod = p * oracle_bf16_to_f32(vr[d]);
-                        a[d] = a[d] + prod;
-                    }
-                }
-                mxc[c] = mx;
-                lc[c] = l;
+                oracle_attention_chunk(q + ((int64_t)m * Hq + h) * D, kc, vc, Hkv, h / g, D, t0, t1, scale, &mxc[c],
+                                       &lc[c], ac + (size_t)c * D);
             }
-            float mx = mxc[0];
-            for (int c = 1; c < C; ++c)
-                if (mxc[c] > mx) mx = mxc[c];
-            float L = 0.0f;
-            for (int c = 0; c < C; ++c) {
-                float w = e_f32(mxc[c] - mx);
-                float wl = w * lc[c];
-                L = L + wl;
-            }
-            for (int d = 0; d < D; ++d) {
-                float num = 0.0f;
-                for (int c = 0; c < C; ++c) {
-                    float w = e_f32(mxc[c] - mx);
-                    float wa = w * ac[(size_t)c * D + d];
-                    num = num + wa;
-                }
-                o[((int64_t)m * Hq + h) * D + d] = oracle_f32_to_bf16_rne(num / L);
-            }
+            oracle_attention_merge(C, mxc, lc, ac, D, o + ((int64_t)m * Hq + h) * D);
             free(mxc);
             free(lc);
             free(ac);
-            free(s);
         }
 }
 

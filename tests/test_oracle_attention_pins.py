@@ -143,3 +143,80 @@ def test_queries_do_not_depend_on_the_batch():
     for m in range(M):
         alone = oracle.attention(q[m:m + 1], k[:T0 + m + 1], v[:T0 + m + 1], T0 + m, 0.125)
         assert np.array_equal(alone[0], o[m])
+
+
+# ---------------------------------------------------------------- fused steps
+
+def _rn32(fr):
+    """Round a Fraction to the nearest fp32, ties to even (exact: the answer is
+    one of the three fp32 values around the double-rounded candidate)."""
+    from fractions import Fraction
+    f = np.float32(float(fr))
+    cands = [np.nextafter(f, np.float32(-np.inf)), f, np.nextafter(f, np.float32(np.inf))]
+    best = min(cands, key=lambda c: (abs(Fraction(float(c)) - fr), int(np.float32(c).view(np.uint32)) & 1))
+    return np.float32(best)
+
+
+def test_exp_matches_two_to_the_rounded_t():
+    """The polynomial part: e(x) is within 3e-7 (relative) of 2^t for the fp32
+    t = x log2(e) it rounds first; a wrong or dropped Taylor term (the x^6 term
+    alone is 2e-6 at |f| = 1/2) fails this."""
+    xs = np.concatenate([-np.logspace(-8, math.log10(87.0), 2000), np.linspace(-87.0, 0.0, 20001)])
+    xs = xs.astype(np.float32)
+    t = xs * np.float32(1.44269502162933349609375)
+    keep = t >= -126.0
+    es = np.array([oracle.attn_exp(float(x)) for x in xs[keep]])
+    ref = np.exp2(t[keep].astype(np.float64))
+    assert np.max(np.abs(es - ref) / ref) <= 3e-7
+
+
+def test_chunk_value_sums_are_fused():
+    """Two positions: q = e_0, k_0 = 0, k_1 = c e_0, so s = (0, c), p = (1, e(c))
+    and l = 1 + e(c); each a_d is then the single rounding of v_0d + e(c) v_1d
+    (a fused multiply-add), computed here in exact rational arithmetic.  Over
+    4096 components some differ from the unfused RN(v_0 + RN(e(c) v_1))."""
+    from fractions import Fraction
+    rng = np.random.default_rng(21)
+    D = 4096
+    q = np.zeros(D, np.uint16)
+    q[0] = 0x3F80                                          # 1.0
+    k = np.zeros((2, 1, D), np.uint16)
+    k[1, 0, 0] = 0xBE99                                    # -0.298828125
+    v = _rand((2, 1, D), rng)
+    mx, l, a = oracle.attention_chunk(q, k, v, 0, 0, 2, 1.0)
+    p1 = np.float32(oracle.attn_exp(float(_f32(0xBE99))))
+    assert mx == 0.0 and l == np.float32(1.0) + p1
+    v0, v1 = _f32(v[0, 0]), _f32(v[1, 0])
+    fused = np.array([_rn32(Fraction(float(x)) + Fraction(float(p1)) * Fraction(float(y))) for x, y in zip(v0, v1)],
+                     np.float32)
+    unfused = v0 + p1 * v1
+    assert np.array_equal(a.view(np.uint32), fused.view(np.uint32))
+    assert np.any(fused != unfused)
+
+
+def test_merge_is_fused_at_a_bf16_tie():
+    """Two chunk results with mx = (0, y), l = (1, 0): w = (1, e(y)), L = 1, and
+    o = bf16(a_0 + e(y) a_1) with one rounding before the bf16 step.  a_0 =
+    1 + 2^-8 is a bf16 tie and e(y) a_1 is just above 2^-24, half an fp32 step
+    at a_0: the fused sum rounds up to a_0 + 2^-23 and the bf16 result to
+    1 + 2^-7 (0x3F81); rounding e(y) a_1 to 2^-24 first would leave the tie
+    and round to 1.0 (0x3F80)."""
+    from fractions import Fraction
+    target = Fraction(1, 2 ** 24)
+    found = None
+    for y in np.linspace(-0.9, -0.1, 81).astype(np.float32):
+        w = np.float32(oracle.attn_exp(float(y)))
+        a1 = np.float32(float(target / Fraction(float(w))))
+        for cand in (a1, np.nextafter(a1, np.float32(np.inf)), np.nextafter(a1, np.float32(2.0))):
+            prod = Fraction(float(w)) * Fraction(float(cand))
+            if target < prod < target * (1 + Fraction(1, 2 ** 25)) and w * cand == np.float32(2.0 ** -24):
+                found = (y, cand)
+                break
+        if found:
+            break
+    assert found is not None
+    y, a1 = found
+    D = 2
+    a = np.array([[1.0 + 2.0 ** -8, 1.0 + 2.0 ** -8], [a1, 0.0]], np.float32)
+    o = oracle.attention_merge(np.array([0.0, y], np.float32), np.array([1.0, 0.0], np.float32), a)
+    assert o[0] == 0x3F81 and o[1] == 0x3F80
