@@ -72,6 +72,8 @@ def parse():
                    help="time only the block-scaled variant and print its figures")
     p.add_argument("--attn-only", action="store_true",
                    help="time only the split-KV verify attention and print its figures")
+    p.add_argument("--attn-cases", default="",
+                   help="with --attn-only: comma-separated M:T0:copies cases (default: the four of the sweep)")
     p.add_argument("--mode", default="program", choices=["program", "calls"],
                    help="program: the step as one verify-pass program launch; calls: one launch per op")
     return p.parse_args()
@@ -398,19 +400,23 @@ def blockq_measure(bi, torch, dev, stream, peaks, Ms=(1, 8, 16)):
     return out
 
 
-def attention_measure(bi, torch, dev, stream, peaks, cases=((8, 4096, 36), (8, 32768, 4), (1, 4096, 36))):
+def attention_measure(bi, torch, dev, stream, peaks, cases=((8, 4096, 36), (8, 32768, 4), (1, 4096, 36),
+                                                            (16, 4096, 36))):
     """The split-KV verify attention of a Qwen3-8B-shaped layer (32 query heads
     over 8 kv heads of 128) through bi_attention_verify, timed alone, for
-    (M queries, T0 cached positions, cache copies): the copies (one per layer
-    of a verify pass) rotate so that each call reads its cache from HBM.
-    Reported: microseconds per call, cache bytes read per second, and the
-    fp32 operations of the fixed-order arithmetic (a multiply and an add per
-    element for the scores and again for the weighted values) per second
-    against the fp32 issue rate of the SMs (152 SMs x 128 lanes x the clock)."""
+    (M queries, T0 cached positions, cache copies).  The copies (one per layer
+    of a verify pass) rotate so that each call reads its cache from HBM; one
+    pass over the copies is captured in a CUDA graph and replayed, so the time
+    is the device's, not the Python caller's.  The path is bound by fp32
+    issue: reported are microseconds per call, cache bytes per second, and
+    the fused multiply-adds of the fixed-order sums (one per element of the
+    scores and one per element of the weighted values: 2 D per query, head
+    and visible position) per second against the SMs' fp32 rate (152 SMs x
+    128 lanes x the 2.07 GHz clock)."""
     import gen
     Hq, Hkv, D = 32, 8, 128
     scale = 1.0 / math.sqrt(D)
-    sm_ops = 152 * 128 * 2.07e9
+    fma_peak = 152 * 128 * 2.07e9
     out = {}
     for M, T0, copies in cases:
         S = T0 + M
@@ -423,28 +429,37 @@ def attention_measure(bi, torch, dev, stream, peaks, cases=((8, 4096, 36), (8, 3
         o = torch.empty((M, Hq, D), dtype=torch.int16, device=dev)
         n = bi.bi_attention_workspace_size(M, Hq, D, T0)
         ws = torch.empty(max(n, 16), dtype=torch.uint8, device=dev)
-        reps = max(2 * copies, 40)
         with torch.cuda.stream(stream):
-            for i in range(2 * copies):
-                bi.bi_attention_verify(q_t, *caches[i % copies], T0, scale, o, ws)
+            for i in range(copies):
+                bi.bi_attention_verify(q_t, *caches[i], T0, scale, o, ws)
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(copies):
+                bi.bi_attention_verify(q_t, *caches[i], T0, scale, o, ws, stream=stream)
+        replays = max(3, 360 // copies)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                g.replay()
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            for i in range(reps):
-                bi.bi_attention_verify(q_t, *caches[i % copies], T0, scale, o, ws)
+            for _ in range(replays):
+                g.replay()
             e1.record(stream)
         stream.synchronize()
-        us = e0.elapsed_time(e1) / reps * 1e3
+        us = e0.elapsed_time(e1) / (replays * copies) * 1e3
         kv_bytes = 2 * S * Hkv * D * 2
-        ops = 4 * D * Hq * sum(T0 + m + 1 for m in range(M))
+        fma = 2 * D * Hq * sum(T0 + m + 1 for m in range(M))
         out["M%d_T%d" % (M, T0)] = {
             "us": round(us, 2), "kv_gbs": round(kv_bytes / (us * 1e-6) / 1e9, 1),
             "frac_of_hbm_copy": round(kv_bytes / (us * 1e-6) / 1e9 / float(peaks["hbm_gbs"]), 4),
-            "fp32_tops": round(ops / (us * 1e-6) / 1e12, 2), "frac_of_fp32_issue": round(ops / (us * 1e-6) / sm_ops, 4),
-            "kv_bytes": kv_bytes, "copies": copies}
-        del caches
+            "fma_tera_per_s": round(fma / (us * 1e-6) / 1e12, 2),
+            "frac_of_fp32_fma_rate": round(fma / (us * 1e-6) / fma_peak, 4),
+            "kv_bytes": kv_bytes, "fma": fma, "copies": copies}
+        del caches, g
     out["note"] = ("Hq=32, Hkv=8, D=128, bf16 q/k/v ~ N(0,1); query m sees positions 0..T0+m; 256-position chunks "
-                   "merged in order; rotating cache copies > L2")
+                   "merged in order; rotating cache copies > L2; CUDA graph of one pass over the copies")
     return out
 
 
@@ -474,7 +489,10 @@ def run_ours(args):
         peaks, _ = read_peaks()
         if rank == 0:
             stream = torch.cuda.Stream(device=dev)
-            print(json.dumps({"attention": attention_measure(bi, torch, dev, stream, peaks)}), flush=True)
+            kw = {}
+            if args.attn_cases:
+                kw["cases"] = tuple(tuple(int(x) for x in c.split(":")) for c in args.attn_cases.split(","))
+            print(json.dumps({"attention": attention_measure(bi, torch, dev, stream, peaks, **kw)}), flush=True)
         return
     t0 = time.time()
     st = Stack(bi, torch, args.layers, dev)

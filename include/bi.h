@@ -303,13 +303,16 @@ BI_API bi_status bi_linear_q6(const int8_t *q, const float *d_a, int M, int K, c
  * t = x log2(e) (fp32 constant 0x3FB8AA3B); 0 if t < -126; else n = rne(t),
  * f = t - n, 2^f by the degree-6 Taylor polynomial of e^(f ln 2) in Horner
  * form with c_0 = 1, c_k = (c_(k-1) ln 2) / k (ln 2 = 0x3F317218), times 2^n.
- * A query's result depends only on its own positions: the same bits for any
- * M, any T0 that leaves it the same cache, and alone or in a batch.
- *   q      bf16 [M, Hq, D]          k, v  bf16 [S, Hkv, D] (k 16-byte aligned)
+ * Every step acc <- acc + x * y is one fused multiply-add.  A query's result
+ * depends only on its own positions: the same bits for any M, for any T0
+ * that leaves it the same cache positions, alone or in a batch.
+ *   q      bf16 [M, Hq, D]          k, v  bf16 [S, Hkv, D]
  *   o      bf16 [M, Hq, D] out      D = 64 or 128; Hq % Hkv == 0; T0 + M <= S
  *   ws     device workspace of at least bi_attention_workspace_size(M, Hq,
- *          D, T0) bytes, 4-byte aligned (null when that size is 0); its
- *          contents need no initialisation and are overwritten.
+ *          D, T0) bytes (null when that size is 0); its contents need no
+ *          initialisation and are overwritten.
+ * Device pointers, all 16-byte aligned; M <= 4096, Hq <= 65535, T0 + M <=
+ * 2^20 positions, M * Hq / Hkv <= 65535 * 32.
  * One or two launches on `stream` (the second merges when the last query
  * covers more than one chunk).  Returns BI_ERR_INVALID_ARG for a null
  * pointer or an out-of-range size, BI_ERR_ALIGNMENT, BI_ERR_WORKSPACE.

@@ -8,10 +8,10 @@ namespace bi {
 
 struct AttnArgs {
     const uint16_t *q;   // [M, Hq, D] bf16
-    const uint16_t *k;   // [S, Hkv, D] bf16, 16-byte aligned
+    const uint16_t *k;   // [S, Hkv, D] bf16 (k, v, o: 16-byte aligned)
     const uint16_t *v;   // [S, Hkv, D] bf16
     uint16_t *o;         // [M, Hq, D] bf16
-    float *ws;           // [M, Hq, Cmax, D + 2] fp32 chunk partials (mx, l, a)
+    float *ws;           // [M, Hq, Cmax, D + 4] fp32 chunk results: mx, l, 2 unused, a[D]
     float scale;
     int M, Hq, Hkv, D, T0, Cmax;
 };

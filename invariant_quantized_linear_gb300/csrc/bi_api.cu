@@ -17,7 +17,9 @@ namespace {
 using bi::kMaxGrid;
 
 constexpr long long kMaxK = 133144;  // largest K with K * 127^2 < 2^31
-constexpr int kMaxAttnQueries = 4096; // queries of one attention call (grid z)
+constexpr int kMaxAttnQueries = 4096;         // queries of one attention call
+constexpr int kMaxAttnPositions = 1 << 20;    // T0 + M: at most 4096 chunks (the merge stages 8 bytes a chunk)
+constexpr long long kMaxAttnRows = 65535LL * 32; // M * Hq / Hkv: 32-row blocks on one grid axis
 
 bool aligned16(const void *p)
 {
@@ -349,11 +351,11 @@ bi_status bi_linear_q6(const int8_t *q, const float *d_a, int M, int K, const ui
 size_t bi_attention_workspace_size(int M, int Hq, int D, int T0)
 {
     if (M < 1 || M > kMaxAttnQueries || Hq < 1 || Hq > 65535 || (D != 64 && D != 128) || T0 < 0 ||
-        T0 > INT32_MAX - M)
+        T0 > kMaxAttnPositions - M)
         return 0;
     const int C = bi::attn_chunks(T0, M);
     if (C == 1) return 0;
-    return static_cast<size_t>(M) * Hq * C * (D + 2) * sizeof(float);
+    return static_cast<size_t>(M) * Hq * C * (D + 4) * sizeof(float);
 }
 
 bi_status bi_attention_verify(const uint16_t *q, const uint16_t *k, const uint16_t *v, int M, int Hq, int Hkv, int D,
@@ -361,14 +363,13 @@ bi_status bi_attention_verify(const uint16_t *q, const uint16_t *k, const uint16
 {
     if (!q || !k || !v || !o) return BI_ERR_INVALID_ARG;
     if (M < 1 || M > kMaxAttnQueries || Hq < 1 || Hq > 65535 || Hkv < 1 || (Hq % Hkv) != 0 ||
-        (D != 64 && D != 128) || T0 < 0 || S < 1 || T0 > S - M || !(scale == scale) || scale == INFINITY ||
+        (D != 64 && D != 128) || T0 < 0 || S < 1 || T0 > S - M || T0 > kMaxAttnPositions - M ||
+        static_cast<long long>(M) * (Hq / Hkv) > kMaxAttnRows || !(scale == scale) || scale == INFINITY ||
         scale == -INFINITY)
         return BI_ERR_INVALID_ARG;
-    if (!aligned16(k) || (reinterpret_cast<uintptr_t>(q) & 1u) || (reinterpret_cast<uintptr_t>(v) & 1u) ||
-        (reinterpret_cast<uintptr_t>(o) & 1u))
-        return BI_ERR_ALIGNMENT;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return BI_ERR_ALIGNMENT;
     const size_t need = bi_attention_workspace_size(M, Hq, D, T0);
-    if (need > 0 && (!ws || ws_bytes < need || !aligned4(ws))) return BI_ERR_WORKSPACE;
+    if (need > 0 && (!ws || ws_bytes < need || !aligned16(ws))) return BI_ERR_WORKSPACE;
     const bi_status st = device_info(nullptr);
     if (st != BI_OK) return st;
     bi::AttnArgs a;

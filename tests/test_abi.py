@@ -178,11 +178,12 @@ def test_block_scaled_validation(bi):
 def test_attention_validation(bi):
     """The split-KV attention: D of 64 or 128, Hq a multiple of Hkv, the last
     query's positions inside the cache, a finite scale, k 16-byte aligned and a
-    workspace once a query covers more than one chunk of 256 positions."""
+    workspace once a query covers more than one chunk of 256 positions; q, k,
+    v, o and the workspace 16-byte aligned."""
     Z = bi.lib.bi_attention_workspace_size
     assert Z(8, 32, 128, 100) == 0                       # 108 positions: one chunk
-    assert Z(8, 32, 128, 1000) == 8 * 32 * 4 * 130 * 4   # 1008 positions: 4 chunks
-    assert Z(1, 1, 64, 256) == 2 * 66 * 4
+    assert Z(8, 32, 128, 1000) == 8 * 32 * 4 * 132 * 4   # 1008 positions: 4 chunks
+    assert Z(1, 1, 64, 256) == 2 * 68 * 4
     assert Z(8, 32, 96, 1000) == 0 and Z(0, 32, 128, 1000) == 0
     F = bi.lib.bi_attention_verify
     args = dict(q=FAKE, k=FAKE, v=FAKE, M=8, Hq=32, Hkv=8, D=128, T0=1000, S=1008, scale=0.088, o=FAKE, ws=None,
@@ -198,10 +199,13 @@ def test_attention_validation(bi):
     assert call(S=1007) == bi.BI_ERR_INVALID_ARG          # T0 + M > S
     assert call(M=0) == bi.BI_ERR_INVALID_ARG
     assert call(T0=-1) == bi.BI_ERR_INVALID_ARG
+    assert call(T0=(1 << 20) - 7, S=(1 << 20) + 1) == bi.BI_ERR_INVALID_ARG   # more than 2^20 positions
+    assert Z(8, 32, 128, (1 << 20) - 7) == 0
     assert call(scale=float("nan")) == bi.BI_ERR_INVALID_ARG
     assert call(scale=float("inf")) == bi.BI_ERR_INVALID_ARG
     assert call(o=None) == bi.BI_ERR_INVALID_ARG
     assert call(k=FAKE + 2) == bi.BI_ERR_ALIGNMENT
     assert call(v=FAKE + 1) == bi.BI_ERR_ALIGNMENT
+    assert call(q=FAKE + 8) == bi.BI_ERR_ALIGNMENT and call(o=FAKE + 4) == bi.BI_ERR_ALIGNMENT
     assert call() == bi.BI_ERR_WORKSPACE                  # 4 chunks, no workspace
     assert call(ws=FAKE, ws_bytes=Z(8, 32, 128, 1000) - 1) == bi.BI_ERR_WORKSPACE
