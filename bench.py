@@ -712,11 +712,23 @@ def cpu_baseline(bounded_s=12.0, M=8):
         if time.time() - t0 >= bounded_s:
             break
     dt = (time.time() - t0) / n
+    total = time.time() - t0
+    # the verify attention of one layer (M = 8 after 4096 positions) on the same cores
+    import gen
+    q, k, v = gen.attn_qkv(gen.ATTENTION_SEED, 8, 32, 8, 128, 4104)
+    ta, na = time.time(), 0
+    while na < 1 or time.time() - ta < 2.0:
+        oracle.attention(q, k, v, 4096, 1.0 / math.sqrt(128))
+        na += 1
+    attn_us = (time.time() - ta) / na * 1e6
     return {"value": round(layer_bytes / dt / 1e9, 3), "unit": UNIT,
             "cores": oracle.num_threads(), "kind": "oracle",
             "sample": "layer 0 of the chained stack (q/k/v, o, gate/up, down with the fused quantisation, "
                       "residual and MLP steps; %d weight bytes) at M=%d, repeated %d times in %.1f s"
-                      % (layer_bytes, M, n, time.time() - t0)}
+                      % (layer_bytes, M, n, total),
+            "attention": {"us": round(attn_us, 1), "calls": na,
+                          "sample": "verify attention of one Qwen3-8B-shaped layer (32/8 heads of 128), M = 8 "
+                                    "after 4096 positions, oracle on the same cores"}}
 
 
 def run_reference(args):

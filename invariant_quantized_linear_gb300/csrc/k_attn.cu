@@ -35,6 +35,7 @@ constexpr int kChunk = 256;       // positions per chunk
 constexpr int kRows = 32;         // (query, q head) rows per chunk CTA
 constexpr int kScoreWarps = 8;    // warps of the score and value tiles
 constexpr int kAttnThreads = 32 * (kScoreWarps + 1);   // + one warp for the weight sums l
+constexpr int kMergeBatch = 16;   // chunk values a merge thread has in flight at once
 
 struct ExpCoef {
     float c[7];
@@ -166,15 +167,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_chunk_kernel(AttnArgs a)
     // q rows (loads issued first), then K; V is staged once K has landed, so
     // that K arrives at full bandwidth and V overlaps the scores
     constexpr int kQPer = (kRows * kSeg + kAttnThreads - 1) / kAttnThreads;
-    uint4 qv[kQPer];
+    uint4 qv[kQPer];                                   // piece i: row i % 32, 16-byte segment i / 32
 #pragma unroll
     for (int k = 0; k < kQPer; ++k) {
-        const int i = tid + k * kAttnThreads, rl = i / kSeg, r = r0 + rl;
+        const int i = tid + k * kAttnThreads, rl = i % kRows, r = r0 + rl;
         qv[k] = make_uint4(0u, 0u, 0u, 0u);
         if (i < kRows * kSeg && r < rows) {
             const int m = r / G, h = hk * G + (r - m * G);
-            qv[k] = __ldg(reinterpret_cast<const uint4 *>(a.q + (static_cast<size_t>(m) * a.Hq + h) * D) +
-                          (i - rl * kSeg));
+            qv[k] = __ldg(reinterpret_cast<const uint4 *>(a.q + (static_cast<size_t>(m) * a.Hq + h) * D) + i / kRows);
         }
     }
     for (int i = tid; i < n_max * kSeg; i += kAttnThreads) {
@@ -184,9 +184,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_chunk_kernel(AttnArgs a)
     cp_async_commit();
 #pragma unroll
     for (int k = 0; k < kQPer; ++k) {
-        const int i = tid + k * kAttnThreads, rl = i / kSeg, sg = i - rl * kSeg;
+        const int i = tid + k * kAttnThreads, rl = i % kRows, sg = i / kRows;
         if (i < kRows * kSeg) {
-            float *dst = Qs + 8 * sg * kRows + rl;     // q as [d][row]
+            float *dst = Qs + 8 * sg * kRows + rl;     // q as [d][row]: a warp's 32 rows hit 32 banks
             const uint32_t w[4] = {qv[k].x, qv[k].y, qv[k].z, qv[k].w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -400,6 +400,9 @@ __global__ void __launch_bounds__(D) attn_merge_kernel(AttnArgs a)
     if (C == 1) return;
     pdl_wait();                                        // the chunk grid has ended and its results are visible
     const float *part = a.ws + (static_cast<size_t>(m) * a.Hq + h) * a.Cmax * (D + 4);
+    float a0[kMergeBatch];                             // the first chunks' values, loaded with the maxima
+#pragma unroll
+    for (int k = 0; k < kMergeBatch; ++k) a0[k] = k < C ? part[static_cast<size_t>(k) * (D + 4) + 4 + d] : 0.0f;
     float mx = -INFINITY;
     for (int c = d; c < C; c += D) {
         const float mc = part[static_cast<size_t>(c) * (D + 4)];
@@ -419,11 +422,19 @@ __global__ void __launch_bounds__(D) attn_merge_kernel(AttnArgs a)
     __syncthreads();
     float L = 0.0f, num = 0.0f;
     const float *pa = part + 4 + d;
-#pragma unroll 8
-    for (int c = 0; c < C; ++c) {
-        const float w = wl[c];
-        L = __fmaf_rn(w, wl[a.Cmax + c], L);
-        num = __fmaf_rn(w, pa[static_cast<size_t>(c) * (D + 4)], num);
+    for (int c0 = 0; c0 < C; c0 += kMergeBatch) {
+        float av[kMergeBatch];
+#pragma unroll
+        for (int k = 0; k < kMergeBatch; ++k)
+            av[k] = c0 == 0 ? a0[k] : c0 + k < C ? pa[static_cast<size_t>(c0 + k) * (D + 4)] : 0.0f;
+#pragma unroll
+        for (int k = 0; k < kMergeBatch; ++k) {
+            if (c0 + k < C) {
+                const float w = wl[c0 + k];
+                L = __fmaf_rn(w, wl[a.Cmax + c0 + k], L);
+                num = __fmaf_rn(w, av[k], num);
+            }
+        }
     }
     a.o[(static_cast<size_t>(m) * a.Hq + h) * D + d] = __bfloat16_as_ushort(__float2bfloat16_rn(__fdiv_rn(num, L)));
 }
