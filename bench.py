@@ -463,6 +463,43 @@ def attention_measure(bi, torch, dev, stream, peaks, cases=((8, 4096, 36), (8, 3
     return out
 
 
+def own_ceilings(bi, torch, dev, stream, read_bytes=4 << 30, copy_bytes=2 << 30, reps=5):
+    """The device's read-only and copy ceilings measured with the library's own
+    probes (16-byte streaming loads, a grid of four 512-thread CTAs per SM),
+    best of `reps`; copy counts read + written bytes like the driver's figure."""
+    buf = torch.zeros(read_bytes, dtype=torch.uint8, device=dev)
+    out = torch.zeros(1, dtype=torch.int64, device=dev)
+    best_r = 0.0
+    with torch.cuda.stream(stream):
+        for i in range(reps + 1):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            bi.bi_probe_read(buf, out, stream=stream)
+            e1.record(stream)
+            e1.synchronize()
+            if i:
+                best_r = max(best_r, read_bytes / (e0.elapsed_time(e1) * 1e-3) / 1e9)
+    del buf
+    src = torch.zeros(copy_bytes, dtype=torch.uint8, device=dev)
+    dst = torch.empty_like(src)
+    best_c = 0.0
+    with torch.cuda.stream(stream):
+        for i in range(reps + 1):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            bi.bi_probe_copy(src, dst, stream=stream)
+            e1.record(stream)
+            e1.synchronize()
+            if i:
+                best_c = max(best_c, 2 * copy_bytes / (e0.elapsed_time(e1) * 1e-3) / 1e9)
+    del src, dst
+    return {"read_gbs": round(best_r, 1), "copy_gbs": round(best_c, 1), "read_bytes": read_bytes,
+            "copy_bytes": copy_bytes,
+            "note": "bi_probe_read / bi_probe_copy, best of %d; copy counts read + written bytes" % reps}
+
+
 def source_sha(path):
     """Hash of a kernel's source and the headers it is built from."""
     h = hashlib.sha256()
@@ -635,6 +672,7 @@ def run_ours(args):
     prefill = prefill_measure(bi, torch, st, stream, peaks) if not args.no_sweep else None
     block_scaled = blockq_measure(bi, torch, dev, stream, peaks) if not args.no_sweep else None
     attention = attention_measure(bi, torch, dev, stream, peaks) if not args.no_sweep else None
+    ceilings = own_ceilings(bi, torch, dev, stream) if not args.no_sweep else None
     cpu = cpu_baseline(bounded_s=12.0) if rank == 0 else None
     if rank == 0:
         line = {
@@ -671,6 +709,8 @@ def run_ours(args):
             "prefill": prefill,
             "block_scaled": block_scaled,
             "attention": attention,
+            "own_ceilings": ceilings,
+            "frac_of_own_read_ceiling": round(achieved / ceilings["read_gbs"], 4) if ceilings else None,
             "setup_s": round(setup_s, 1),
         }
         print(json.dumps(line), flush=True)

@@ -323,6 +323,20 @@ BI_API bi_status bi_attention_verify(const uint16_t *q, const uint16_t *k, const
                                      bi_stream_t stream);
 
 /*
+ * Bandwidth probes, for measurement only: the device's own read-only and copy
+ * ceilings with 16-byte streaming loads (8 in flight per thread) over a grid
+ * of four 512-thread CTAs per SM.  A weight stream only reads, so the
+ * read-only ceiling is the one it is measured against.
+ *   bi_probe_read: reads `bytes` of `buf` once; *out (device, 8-byte aligned)
+ *     = the xor of all its 64-bit words (a check that every byte was read).
+ *   bi_probe_copy: dst = src, `bytes` bytes; src and dst must not overlap.
+ * Device pointers, 16-byte aligned; bytes a positive multiple of 16.
+ * Returns BI_ERR_INVALID_ARG or BI_ERR_ALIGNMENT for bad arguments.
+ */
+BI_API bi_status bi_probe_read(const void *buf, size_t bytes, unsigned long long *out, bi_stream_t stream);
+BI_API bi_status bi_probe_copy(const void *src, void *dst, size_t bytes, bi_stream_t stream);
+
+/*
  * Exhaustive check of the quotient the verify-pass executor quantises with.
  * Codes are clamp(rne(v / s), -127, 127) with v / s an IEEE fp32 division
  * (the per-token absmax quantisation of the W8A8 page, "Quantization").  The

@@ -67,6 +67,10 @@ lib.bi_attention_workspace_size.restype = _sz
 lib.bi_attention_verify.argtypes = [_vp, _vp, _vp, _ci, _ci, _ci, _ci, _ci, _ci, ctypes.c_float, _vp, _vp, _sz,
                                     _vp]
 lib.bi_attention_verify.restype = _ci
+lib.bi_probe_read.argtypes = [_vp, _sz, _vp, _vp]
+lib.bi_probe_read.restype = _ci
+lib.bi_probe_copy.argtypes = [_vp, _vp, _sz, _vp]
+lib.bi_probe_copy.restype = _ci
 
 lib.bi_program_bytes.argtypes = [_ci]
 lib.bi_program_bytes.restype = _sz
@@ -235,6 +239,18 @@ def bi_attention_verify(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, T0: i
     nbytes = 0 if ws is None else ws.numel() * ws.element_size()
     _check(lib.bi_attention_verify(_ptr(q), _ptr(k), _ptr(v), M, Hq, Hkv, D, T0, S, scale, _ptr(o), _ptr(ws),
                                    nbytes, _stream(stream)), "bi_attention_verify")
+
+
+def bi_probe_read(buf: torch.Tensor, out: torch.Tensor, stream=None) -> None:
+    """Read all of `buf` once (bandwidth probe); out: int64 device tensor, receives the xor of its 64-bit words."""
+    _check(lib.bi_probe_read(_ptr(buf), buf.numel() * buf.element_size(), _ptr(out), _stream(stream)),
+           "bi_probe_read")
+
+
+def bi_probe_copy(src: torch.Tensor, dst: torch.Tensor, stream=None) -> None:
+    """dst = src (bandwidth probe), same byte size, not overlapping."""
+    _check(lib.bi_probe_copy(_ptr(src), _ptr(dst), src.numel() * src.element_size(), _stream(stream)),
+           "bi_probe_copy")
 
 
 def bi_linear_w8a8_noalloc(q: torch.Tensor, s_a: torch.Tensor, w_q: torch.Tensor, s_w: torch.Tensor,

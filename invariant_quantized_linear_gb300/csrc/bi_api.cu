@@ -4,6 +4,7 @@
 #include "attn.cuh"
 #include "bi.h"
 #include "blockq.cuh"
+#include "probe.cuh"
 #include "kernels.cuh"
 #include "ptx.cuh"
 
@@ -386,6 +387,28 @@ bi_status bi_attention_verify(const uint16_t *q, const uint16_t *k, const uint16
     a.T0 = T0;
     a.Cmax = bi::attn_chunks(T0, M);
     return from_cuda(bi::launch_attention(a, stream));
+}
+
+bi_status bi_probe_read(const void *buf, size_t bytes, unsigned long long *out, bi_stream_t stream)
+{
+    if (!buf || !out || bytes == 0 || (bytes & 15u) != 0 || (reinterpret_cast<uintptr_t>(out) & 7u) != 0)
+        return BI_ERR_INVALID_ARG;
+    if (!aligned16(buf)) return BI_ERR_ALIGNMENT;
+    const bi_status st = device_info(nullptr);
+    if (st != BI_OK) return st;
+    return from_cuda(bi::launch_probe_read(static_cast<const uint4 *>(buf), bytes / 16, out, stream));
+}
+
+bi_status bi_probe_copy(const void *src, void *dst, size_t bytes, bi_stream_t stream)
+{
+    if (!src || !dst || bytes == 0 || (bytes & 15u) != 0) return BI_ERR_INVALID_ARG;
+    if (!aligned16(src) || !aligned16(dst)) return BI_ERR_ALIGNMENT;
+    const char *s = static_cast<const char *>(src), *d = static_cast<const char *>(dst);
+    if (s < d + bytes && d < s + bytes) return BI_ERR_INVALID_ARG;     // the copy must not overlap
+    const bi_status st = device_info(nullptr);
+    if (st != BI_OK) return st;
+    return from_cuda(bi::launch_probe_copy(static_cast<const uint4 *>(src), static_cast<uint4 *>(dst), bytes / 16,
+                                           stream));
 }
 
 bi_status bi_selftest_quotient(unsigned long long *out, bi_stream_t stream)

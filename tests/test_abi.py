@@ -209,3 +209,18 @@ def test_attention_validation(bi):
     assert call(q=FAKE + 8) == bi.BI_ERR_ALIGNMENT and call(o=FAKE + 4) == bi.BI_ERR_ALIGNMENT
     assert call() == bi.BI_ERR_WORKSPACE                  # 4 chunks, no workspace
     assert call(ws=FAKE, ws_bytes=Z(8, 32, 128, 1000) - 1) == bi.BI_ERR_WORKSPACE
+
+
+def test_probe_validation(bi):
+    """The bandwidth probes: a positive multiple of 16 bytes, 16-byte aligned
+    buffers, an 8-byte aligned result word, no overlapping copy."""
+    R = bi.lib.bi_probe_read
+    assert R(FAKE, 0, FAKE, None) == bi.BI_ERR_INVALID_ARG
+    assert R(FAKE, 100, FAKE, None) == bi.BI_ERR_INVALID_ARG
+    assert R(FAKE, 4096, FAKE + 4, None) == bi.BI_ERR_INVALID_ARG
+    assert R(FAKE + 8, 4096, FAKE, None) == bi.BI_ERR_ALIGNMENT
+    assert R(None, 4096, FAKE, None) == bi.BI_ERR_INVALID_ARG
+    C = bi.lib.bi_probe_copy
+    assert C(FAKE, FAKE + 4096, 8192, None) == bi.BI_ERR_INVALID_ARG      # overlapping
+    assert C(FAKE, FAKE + 8192, 24, None) == bi.BI_ERR_INVALID_ARG
+    assert C(FAKE + 4, FAKE + 8192, 4096, None) == bi.BI_ERR_ALIGNMENT
