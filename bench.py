@@ -510,6 +510,22 @@ def source_sha(path):
     return h.hexdigest()
 
 
+def reduce_max(x, world, device):
+    """The largest x over all ranks (x itself on one rank): the job's time is
+    its slowest rank's."""
+    if world <= 1:
+        return x
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(bytes_per_rank, world, ms):
+    """Whole-job GB/s: every rank streams bytes_per_rank in ms (the max over ranks)."""
+    return bytes_per_rank * world / (ms * 1e-3) / 1e9
+
+
 def run_ours(args):
     import torch
     rank, world, local = dist_env()
@@ -591,18 +607,13 @@ def run_ours(args):
             e1.record(stream)
         barrier()
         region["t1"] = time.monotonic()
-        ms = e0.elapsed_time(e1) / steps
-        if world > 1:
-            t = torch.tensor([ms], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            ms = float(t.item())
-        return ms
+        return reduce_max(e0.elapsed_time(e1) / steps, world, dev)
 
     g = graph_for(M)
     clocks = ClockSampler(local)
     ms = time_graph(g, args.steps, args.warmup)
     clk = clocks.stop(region["t0"], region["t1"])
-    gbs = st.weight_bytes * world / (ms * 1e-3) / 1e9
+    gbs = job_rate(st.weight_bytes, world, ms)
 
     # per-M sweep (same step, fewer repetitions)
     per_m = {}
@@ -658,8 +669,8 @@ def run_ours(args):
             host_acc.copy_(st.accept, non_blocking=True)
         e1.record(stream)
     barrier()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    e2e_gbs = st.weight_bytes * world / (e2e_ms * 1e-3) / 1e9
+    e2e_ms = reduce_max(e0.elapsed_time(e1) / e2e_steps, world, dev)
+    e2e_gbs = job_rate(st.weight_bytes, world, e2e_ms)
 
     peaks, kind = read_peaks()
     peak = float(peaks["hbm_gbs"])
