@@ -132,8 +132,8 @@ __device__ __forceinline__ int chunk_positions(int T0, int m, int c)
 // K and V rows are staged once in shared memory and shared by all the rows.
 // Sums run as packed pairs of independent fmas (fma.rn.f32x2), each lane the
 // same correctly rounded step as a scalar fma.
-//   scores: warp w < 8 holds rows 8 (w & 3) .. +7 (as 4 row pairs) at
-//           positions 128 (w >> 2) + lane + 32 j (j < 4); sum over d in order.
+//   scores: warp w < 8 holds rows 8 (w >> 1) .. +7 (as 4 row pairs) at
+//           positions 128 (w & 1) + lane + 32 j (j < 4); sum over d in order.
 //   values: warp w < 8 holds rows 4 w .. +3 at d = (D / 32) lane .. (pairs
 //           of adjacent d); sum over positions in order.
 //   l:      warp 8 sums the weights of row lane in position order meanwhile.
@@ -206,7 +206,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_chunk_kernel(AttnArgs a)
 
     // ---- scores of 8 rows x 4 positions per thread
     const bool scorer = warp < kScoreWarps;
-    const int rg = warp & 3, pg = (warp >> 2) & 1;
+    const int rg = (warp >> 1) & 3, pg = warp & 1;     // a row group's two warps sit on two partitions
     const int rs0 = r0 + 8 * rg;                       // first row of this warp's score tile
     float s[8][4];
     if (scorer && rs0 < rows) {
