@@ -91,22 +91,42 @@ __global__ void quantize_act_blocks_kernel(const uint16_t *__restrict__ x, int64
     if (lane == 0) d_a[static_cast<long long>(m) * nb + b] = s;
 }
 
-// 32 codes of one 32-block as signed bytes, four per word in element order:
-// the low nibbles of 16 ql bytes and the 2-bit fields of 8 qh bytes.
-__device__ __forceinline__ void unpack32(uint4 l, uint2 h, uint32_t (&c)[8])
+// 32 codes of one 32-block as unsigned bytes u = c + 32 in [0, 63], four per
+// word in element order.  Low nibbles: each ql word holds elements 8t .. 8t+7
+// (even ones in the low nibbles); masking gives the even and the odd
+// elements, and two byte permutes interleave them.  High bits: each qh word
+// holds elements 16s .. 16s+15 as 2-bit fields; four masked shifts put field j
+// of every byte at bits 4-5, and byte permutes gather them in element order.
+__device__ __forceinline__ void unpack32u(uint4 l, uint2 h, uint32_t (&u)[8])
 {
     const uint32_t lw[4] = {l.x, l.y, l.z, l.w};
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        const uint32_t lo = lw[t] & 0x0F0F0F0Fu, hi = (lw[t] >> 4) & 0x0F0F0F0Fu;
+        u[2 * t] = __byte_perm(lo, hi, 0x5140);
+        u[2 * t + 1] = __byte_perm(lo, hi, 0x7362);
+    }
     const uint32_t hw[2] = {h.x, h.y};
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        // elements 4i .. 4i + 3: ql bytes 2i, 2i + 1 (two nibbles each), qh byte i
-        const uint32_t b2 = (lw[i >> 1] >> (16 * (i & 1))) & 0xFFFFu;
-        uint32_t u = (b2 & 0xFu) | ((b2 & 0xF0u) << 4) | ((b2 & 0xF00u) << 8) | ((b2 & 0xF000u) << 12);
-        const uint32_t hb = (hw[i >> 2] >> (8 * (i & 3))) & 0xFFu;
-        u |= ((hb & 3u) << 4) | ((hb & 0xCu) << 10) | ((hb & 0x30u) << 16) | ((hb & 0xC0u) << 22);
-        // u holds c + 32 in [0, 63] per byte: c = u - 32, sign-extended to 8 bits
-        c[i] = (u & 0x1F1F1F1Fu) | ((~u & 0x20202020u) * 7u);
+    for (int q = 0; q < 2; ++q) {
+        const uint32_t w = hw[q];
+        const uint32_t t0 = (w << 4) & 0x30303030u, t1 = (w << 2) & 0x30303030u;
+        const uint32_t t2 = w & 0x30303030u, t3 = (w >> 2) & 0x30303030u;
+        const uint32_t a01 = __byte_perm(t0, t1, 0x5140), a23 = __byte_perm(t2, t3, 0x5140);
+        const uint32_t b01 = __byte_perm(t0, t1, 0x7362), b23 = __byte_perm(t2, t3, 0x7362);
+        u[4 * q + 0] |= __byte_perm(a01, a23, 0x5410);
+        u[4 * q + 1] |= __byte_perm(a01, a23, 0x7632);
+        u[4 * q + 2] |= __byte_perm(b01, b23, 0x5410);
+        u[4 * q + 3] |= __byte_perm(b01, b23, 0x7632);
     }
+}
+
+// sum over 4 byte pairs of (unsigned a byte) * (signed b byte), plus c
+__device__ __forceinline__ int dp4a_us(uint32_t a, int b, int c)
+{
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
 }
 
 // The stored weight data of one 32-block of one row.
@@ -165,9 +185,9 @@ __global__ void __launch_bounds__(kLinWarps * 32) linear_q6_kernel(const int8_t 
 #pragma unroll
             for (int r = 0; r < R; ++r) nxt[r] = load_block(ql, qh, sc, d, min(n0 + r, N - 1), K, b + 32);
         }
-        uint32_t c[R][8];
+        uint32_t u[R][8];                              // codes + 32, unsigned
 #pragma unroll
-        for (int r = 0; r < R; ++r) unpack32(cur[r].l, cur[r].h, c[r]);
+        for (int r = 0; r < R; ++r) unpack32u(cur[r].l, cur[r].h, u[r]);
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
             if (m >= M) break;
@@ -177,15 +197,22 @@ __global__ void __launch_bounds__(kLinWarps * 32) linear_q6_kernel(const int8_t 
             const int a[8] = {static_cast<int>(a0.x), static_cast<int>(a0.y), static_cast<int>(a0.z),
                               static_cast<int>(a0.w), static_cast<int>(a1.x), static_cast<int>(a1.y),
                               static_cast<int>(a1.z), static_cast<int>(a1.w)};
+            // sum(c a) = sum(u a) - 32 sum(a) per sub-block of 16: the same integer
+            int as0 = 0, as1 = 0;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                as0 = __dp4a(0x01010101, a[k], as0);
+                as1 = __dp4a(0x01010101, a[4 + k], as1);
+            }
 #pragma unroll
             for (int r = 0; r < R; ++r) {
                 int s0 = 0, s1 = 0;
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    s0 = __dp4a(static_cast<int>(c[r][k]), a[k], s0);
-                    s1 = __dp4a(static_cast<int>(c[r][4 + k]), a[4 + k], s1);
+                    s0 = dp4a_us(u[r][k], a[k], s0);
+                    s1 = dp4a_us(u[r][4 + k], a[4 + k], s1);
                 }
-                const int isum = cur[r].s.x * s0 + cur[r].s.y * s1;
+                const int isum = cur[r].s.x * (s0 - 32 * as0) + cur[r].s.y * (s1 - 32 * as1);
                 const float v = __fmul_rn(__fmul_rn(__int2float_rn(isum), da), cur[r].d);
                 p[m][r] = __fadd_rn(p[m][r], v);
             }
