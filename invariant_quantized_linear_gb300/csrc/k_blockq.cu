@@ -154,13 +154,10 @@ __device__ __forceinline__ BlockW load_block(const uint8_t *__restrict__ ql, con
 // current one is computed), and each activation block is loaded once for the
 // warp's R rows.  MT and R change the work per thread, not the adds.
 template <int MT, int R>
-__global__ void __launch_bounds__(kLinWarps * 32) linear_q6_kernel(const int8_t *__restrict__ qa,
-                                                                   const float *__restrict__ d_a, int M, int K,
-                                                                   const uint8_t *__restrict__ ql,
-                                                                   const uint8_t *__restrict__ qh,
-                                                                   const int8_t *__restrict__ sc,
-                                                                   const float *__restrict__ d, int N, float *y,
-                                                                   int pdl)
+__device__ __forceinline__ void linear_q6_body(const int8_t *__restrict__ qa, const float *__restrict__ d_a, int M,
+                                               int K, const uint8_t *__restrict__ ql, const uint8_t *__restrict__ qh,
+                                               const int8_t *__restrict__ sc, const float *__restrict__ d, int N,
+                                               float *y, int pdl)
 {
     if (pdl) {
         pdl_launch_dependents();
@@ -234,6 +231,30 @@ __global__ void __launch_bounds__(kLinWarps * 32) linear_q6_kernel(const int8_t 
 }
 
 template <int MT, int R>
+__global__ void __launch_bounds__(kLinWarps * 32) linear_q6_kernel(const int8_t *__restrict__ qa,
+                                                                   const float *__restrict__ d_a, int M, int K,
+                                                                   const uint8_t *__restrict__ ql,
+                                                                   const uint8_t *__restrict__ qh,
+                                                                   const int8_t *__restrict__ sc,
+                                                                   const float *__restrict__ d, int N, float *y,
+                                                                   int pdl)
+{
+    linear_q6_body<MT, R>(qa, d_a, M, K, ql, qh, sc, d, N, y, pdl);
+}
+
+// One token: fewer live registers, so more warps per SM keep weight loads in flight.
+__global__ void __launch_bounds__(kLinWarps * 32, 5) linear_q6_kernel_m1(const int8_t *__restrict__ qa,
+                                                                         const float *__restrict__ d_a, int M, int K,
+                                                                         const uint8_t *__restrict__ ql,
+                                                                         const uint8_t *__restrict__ qh,
+                                                                         const int8_t *__restrict__ sc,
+                                                                         const float *__restrict__ d, int N, float *y,
+                                                                         int pdl)
+{
+    linear_q6_body<1, 1>(qa, d_a, M, K, ql, qh, sc, d, N, y, pdl);
+}
+
+template <int MT, int R>
 cudaError_t launch_q6(const int8_t *qa, const float *d_a, int M, int K, const uint8_t *ql, const uint8_t *qh,
                       const int8_t *sc, const float *d, int N, float *y, bool pdl, cudaStream_t stream)
 {
@@ -247,7 +268,10 @@ cudaError_t launch_q6(const int8_t *qa, const float *d_a, int M, int K, const ui
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, linear_q6_kernel<MT, R>, qa, d_a, M, K, ql, qh, sc, d, N, y, pdl ? 1 : 0);
+    if constexpr (MT == 1)
+        return cudaLaunchKernelEx(&cfg, linear_q6_kernel_m1, qa, d_a, M, K, ql, qh, sc, d, N, y, pdl ? 1 : 0);
+    else
+        return cudaLaunchKernelEx(&cfg, linear_q6_kernel<MT, R>, qa, d_a, M, K, ql, qh, sc, d, N, y, pdl ? 1 : 0);
 }
 
 }  // namespace
@@ -273,6 +297,7 @@ cudaError_t launch_linear_q6(const int8_t *qa, const float *d_a, int M, int K, c
 {
     // one row per warp at M <= 4; two above, where each activation load then
     // serves two rows (measured best of one, two and four rows per warp)
+    if (M == 1) return launch_q6<1, 1>(qa, d_a, M, K, ql, qh, sc, d, N, y, pdl, stream);
     if (M <= 4) return launch_q6<4, 1>(qa, d_a, M, K, ql, qh, sc, d, N, y, pdl, stream);
     if (M <= 8) return launch_q6<8, 2>(qa, d_a, M, K, ql, qh, sc, d, N, y, pdl, stream);
     return launch_q6<16, 2>(qa, d_a, M, K, ql, qh, sc, d, N, y, pdl, stream);
