@@ -220,3 +220,20 @@ def test_merge_is_fused_at_a_bf16_tie():
     a = np.array([[1.0 + 2.0 ** -8, 1.0 + 2.0 ** -8], [a1, 0.0]], np.float32)
     o = oracle.attention_merge(np.array([0.0, y], np.float32), np.array([1.0, 0.0], np.float32), a)
     assert o[0] == 0x3F81 and o[1] == 0x3F80
+
+
+def test_equal_scores_across_chunks_give_the_rounded_mean():
+    """q = 0 over 700 positions (three chunks): every weight is 1, every chunk
+    maximum 0, so every merge weight is e(0) = 1; with small integer values all
+    sums are exact and o is bf16(RN32(sum(v) / 700)), the rounded mean."""
+    from fractions import Fraction
+    rng = np.random.default_rng(8)
+    D, T = 16, 700
+    vals = rng.integers(-8, 9, (T, 1, D)).astype(np.float32)
+    v = _bf16_bits(vals)
+    k = _rand((T, 1, D), rng)
+    q = _bf16_bits(np.zeros((1, 1, D)))
+    o = oracle.attention(q, k, v, T - 1, 0.125)
+    for d in range(D):
+        mean = _rn32(Fraction(int(vals[:, 0, d].sum()), T))
+        assert o[0, 0, d] == _bf16_bits(np.float32(mean))
