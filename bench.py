@@ -772,8 +772,17 @@ def cpu_baseline(bounded_s=12.0, M=8):
         oracle.attention(q, k, v, 4096, 1.0 / math.sqrt(128))
         na += 1
     attn_us = (time.time() - ta) / na * 1e6
+    # the same layer on one thread, bounded to a few seconds
+    cores = oracle.num_threads()
+    oracle.set_num_threads(1)
+    t1, n1 = time.time(), 0
+    while n1 < 1 or time.time() - t1 < 3.0:
+        _oracle_layer(oracle, L, h0, M)
+        n1 += 1
+    one_thread = layer_bytes / ((time.time() - t1) / n1) / 1e9
+    oracle.set_num_threads(cores)
     return {"value": round(layer_bytes / dt / 1e9, 3), "unit": UNIT,
-            "cores": oracle.num_threads(), "kind": "oracle",
+            "cores": cores, "kind": "oracle", "one_thread_value": round(one_thread, 3),
             "sample": "layer 0 of the chained stack (q/k/v, o, gate/up, down with the fused quantisation, "
                       "residual and MLP steps; %d weight bytes) at M=%d, repeated %d times in %.1f s"
                       % (layer_bytes, M, n, total),

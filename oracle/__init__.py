@@ -62,6 +62,8 @@ def lib():
         L.oracle_attention_merge.restype = None
         L.oracle_num_threads.argtypes = []
         L.oracle_num_threads.restype = ci
+        L.oracle_set_num_threads.argtypes = [ci]
+        L.oracle_set_num_threads.restype = None
         _LIB = L
     return _LIB
 
@@ -321,3 +323,8 @@ def attention_merge(mx, l, a) -> np.ndarray:
 
 def num_threads() -> int:
     return int(lib().oracle_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """Threads of the parallel loops (results do not depend on it)."""
+    lib().oracle_set_num_threads(int(n))

@@ -592,3 +592,15 @@ int oracle_num_threads(void)
     return 1;
 #endif
 }
+
+/* Threads for the parallel loops above (timing only: every result is the same
+ * for any thread count, each output element being computed by one thread). */
+void oracle_set_num_threads(int n)
+{
+#ifdef _OPENMP
+    extern void omp_set_num_threads(int);
+    omp_set_num_threads(n > 0 ? n : 1);
+#else
+    (void)n;
+#endif
+}
