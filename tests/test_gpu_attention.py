@@ -124,3 +124,17 @@ def test_long_context_sampled_heads(bi):
         g = h // (Hq // Hkv)
         want = oracle.attention(q[:, h:h + 1], k[:, g:g + 1], v[:, g:g + 1], T0, scale)
         _assert_same(o[:, h:h + 1], want)
+
+
+def test_maximum_positions(bi):
+    """The largest cache the entry point takes: T0 + M = 2^20 positions (4096
+    chunks, the widest merge), two queries, 8 q heads over one kv head; two
+    sampled heads equal the oracle's."""
+    M, Hq, Hkv, D = 2, 8, 1, 128
+    T0 = (1 << 20) - M
+    q, k, v = gen.attn_qkv(29, M, Hq, Hkv, D, T0 + M)
+    scale = 1.0 / math.sqrt(D)
+    o = _attn_gpu(bi, q, k, v, T0, scale)
+    for h in (0, 5):
+        want = oracle.attention(q[:, h:h + 1], k, v, T0, scale)
+        _assert_same(o[:, h:h + 1], want)
