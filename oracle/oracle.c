@@ -1,12 +1,16 @@
 /*
- * CPU oracle for the batch-invariant W8A8 verify-pass linear layer.
+ * CPU oracle for the batch-invariant verify pass: the W8A8 linear layer and
+ * LM-head argmax, the chained pass's elementwise steps, the block-scaled
+ * variant and the split-KV attention of the verify queries.
  *
  * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the
  * benchmark's CPU-baseline leg may load this file's library.  It shares no
  * code, header or table with the CUDA library and calls nothing in it.
  *
  * Plain scalar C, built with -O2 -ffp-contract=off and no fast-math, so every
- * float operation below is one IEEE-754 operation rounded to nearest-even.
+ * float operation below is one IEEE-754 operation rounded to nearest-even; an
+ * explicit fmaf (the attention's multiply-accumulate steps) is one fused
+ * operation with one rounding.
  * Sums of int8 products are carried in int64 (exact) and checked against the
  * int32 range.  Loops run in the textbook order; the only parallelism is an
  * OpenMP loop over independent output elements, which cannot change a result.
