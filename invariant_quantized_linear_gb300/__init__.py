@@ -1,4 +1,6 @@
-"""Batch-invariant W8A8 linear layer for GB300 (sm_103a): Python binding.
+"""Batch-invariant verify pass for GB300 (sm_103a): Python binding of the W8A8
+linear and LM head, the verify-pass executor, the block-scaled variant and the
+split-KV verify attention.
 
 A thin ctypes layer over ``libbi.so`` (C ABI declared in ``include/bi.h``).
 Each function has the name of the C entry point it calls and only marshals
