@@ -1,10 +1,12 @@
 /*
- * bi.h - batch-invariant W8A8 linear layer for GB300 (sm_103a), C ABI.
+ * bi.h - batch-invariant verify pass for GB300 (sm_103a), C ABI.
  *
  * The library computes the linear layers of an LLM decode or speculative
  * verify pass (M = 1 .. K+1 tokens against a large int8 weight matrix) so that
  * every output row is bitwise identical whatever M is and whatever else shares
- * the pass.  Greedy speculative decoding then keeps exactly the target's own
+ * the pass; with them the LM-head argmax, greedy verification, a block-scaled
+ * variant of the linear and the verify queries' split-KV attention, each with
+ * the same guarantee.  Greedy speculative decoding then keeps exactly the target's own
  * argmax ("why speculative decoding changed my output", introduction: the
  * guarantee needs a position's logits inside a batch to equal its logits
  * decoded alone).
