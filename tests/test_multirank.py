@@ -1,6 +1,7 @@
 """The N > 1 path of the benchmark's host logic on CPU: two gloo ranks, each
 with its own time; every rank gets the slowest rank's time, and the whole-job
 rate counts the bytes of both ranks against it (replicas, no data exchange)."""
+import datetime
 import os
 import socket
 import sys
@@ -22,7 +23,7 @@ def _rank(rank, world, port, out):
     sys.path.insert(0, ROOT)
     import bench
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
-    dist.init_process_group("gloo", rank=rank, world_size=world)
+    dist.init_process_group("gloo", rank=rank, world_size=world, timeout=datetime.timedelta(seconds=60))
     try:
         ms = [2.5, 3.25][rank]                       # rank 1 is the slower one
         got = bench.reduce_max(ms, world, "cpu")
