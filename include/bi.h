@@ -234,8 +234,10 @@ BI_API bi_status bi_greedy_verify(const int32_t *argmax, const int32_t *draft, i
  * bounded wait the kernels use, on a barrier phase that nothing completes.
  * After the wait limit (2 s of GPU time) it gives up and sets the status
  * word of `ws` (a linear workspace, >= bi_linear_workspace_size(1, 1, 16)
- * bytes), so that bi_workspace_status then returns BI_ERR_TIMEOUT.  Nothing
- * faults or hangs; the context stays usable.
+ * bytes), so that bi_workspace_status then returns BI_ERR_TIMEOUT.  With
+ * ws = NULL (ws_bytes ignored) the status word is that of the fixed scratch
+ * of bi_linear_w8a8_noalloc, read back by bi_linear_w8a8_noalloc_status.
+ * Nothing faults or hangs; the context stays usable.
  */
 BI_API bi_status bi_selftest_wait_timeout(void *ws, size_t ws_bytes, bi_stream_t stream);
 
@@ -426,24 +428,36 @@ BI_API bi_status bi_program_run(const void *program, int max_tokens, void *ws, s
  * inside the library, present on every GPU that loads the library until the
  * process exits.  The caller still passes all inputs and outputs.
  *
- *   Arguments, layouts, results and the other errors are those of
- *   bi_linear_w8a8; there is no workspace argument.
+ *   Arguments, layouts, results and the errors found before any launch are
+ *   those of bi_linear_w8a8; there is no workspace argument.
  *   M must be <= BI_NOALLOC_MAX_M (the most the fixed scratch holds); larger
  *   M returns BI_ERR_UNSUPPORTED without launching anything.
- *   The first call on each device looks up the scratch array's device address
- *   (with that device current); make that first call before any stream
- *   capture.
- *   Every call shares the one array: the call clears the parts that must
- *   start at zero (two cudaMemsetAsync on `stream`) and then launches.  Calls
- *   that may overlap on the GPU (other streams, other host threads) race on
- *   the array and must not be issued; calls in order on one stream are fine.
+ *   The first call on each device (and the first after the device's context
+ *   was replaced, for instance by cudaDeviceReset) looks up the scratch
+ *   array's device address with that device current; make that first call
+ *   before any stream capture.
+ *   Every call shares the one array.  The kernel leaves the scratch's counters
+ *   and partial sums at zero when it completes, so a call launches with no
+ *   clearing (BI_FLAG_PDL keeps its effect).  Calls that may overlap on the
+ *   GPU (other streams, other host threads) race on the array and must not
+ *   be issued; calls in order on one stream are fine.
+ *   A wait inside the kernel that gives up (after 2 s) is recorded in the
+ *   scratch's status word and leaves y partly written; later calls are then
+ *   not reliable until bi_linear_w8a8_noalloc_status has reported it.
  *   Results are bitwise identical to bi_linear_w8a8.
+ *
+ * bi_linear_w8a8_noalloc_status: waits for `stream`, then reads the status
+ * word of the scratch on the current device: BI_OK, or BI_ERR_TIMEOUT if a
+ * wait of an earlier call (or of bi_selftest_wait_timeout with a NULL
+ * workspace) gave up.  After a timeout it restores the whole scratch to zero,
+ * so that the next call is reliable again.  Allocates nothing.
  */
 #define BI_NOALLOC_MAX_M 16
 #define BI_NOALLOC_SCRATCH_BYTES 1082624
 BI_API bi_status bi_linear_w8a8_noalloc(const int8_t *q, const float *s_a, int M, int K,
                                         const int8_t *w_q, const float *s_w, int N,
                                         uint16_t *y, unsigned flags, bi_stream_t stream);
+BI_API bi_status bi_linear_w8a8_noalloc_status(bi_stream_t stream);
 
 #ifdef __cplusplus
 }

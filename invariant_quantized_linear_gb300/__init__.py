@@ -58,6 +58,8 @@ lib.bi_workspace_status.argtypes = [_vp, _sz, _vp]
 lib.bi_workspace_status.restype = _ci
 lib.bi_linear_w8a8_noalloc.argtypes = [_vp, _vp, _ci, _ci, _vp, _vp, _ci, _vp, _cu, _vp]
 lib.bi_linear_w8a8_noalloc.restype = _ci
+lib.bi_linear_w8a8_noalloc_status.argtypes = [_vp]
+lib.bi_linear_w8a8_noalloc_status.restype = _ci
 lib.bi_quantize_weight_q6.argtypes = [_vp, _i64, _ci, _ci, _vp, _vp, _vp, _vp, _vp]
 lib.bi_quantize_weight_q6.restype = _ci
 lib.bi_quantize_act_blocks.argtypes = [_vp, _i64, _ci, _ci, _vp, _vp, _vp]
@@ -264,6 +266,12 @@ def bi_linear_w8a8_noalloc(q: torch.Tensor, s_a: torch.Tensor, w_q: torch.Tensor
     N = w_q.shape[0]
     _check(lib.bi_linear_w8a8_noalloc(_ptr(q), _ptr(s_a), M, K, _ptr(w_q), _ptr(s_w), N, _ptr(y), flags,
                                       _stream(stream)), "bi_linear_w8a8_noalloc")
+
+
+def bi_linear_w8a8_noalloc_status(stream=None) -> int:
+    """Status of the no-alloc entry point's scratch after `stream`: BI_OK, or
+    BI_ERR_TIMEOUT (once; the scratch is then restored)."""
+    return int(lib.bi_linear_w8a8_noalloc_status(_stream(stream)))
 
 
 def bi_program_bytes(n_ops: int) -> int:

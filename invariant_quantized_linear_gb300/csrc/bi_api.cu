@@ -5,6 +5,7 @@
 #include "bi.h"
 #include "blockq.cuh"
 #include "probe.cuh"
+#include "host_common.h"
 #include "kernels.cuh"
 #include "ptx.cuh"
 
@@ -16,21 +17,15 @@
 namespace {
 
 using bi::kMaxGrid;
+using bi::host::aligned16;
+using bi::host::aligned4;
+using bi::host::check_k;
+using bi::host::device_info;
+using bi::host::encode_int8_2d;
 
-constexpr long long kMaxK = 133144;  // largest K with K * 127^2 < 2^31
 constexpr int kMaxAttnQueries = 4096;         // queries of one attention call
 constexpr int kMaxAttnPositions = 1 << 20;    // T0 + M: at most 4096 chunks (the merge stages 8 bytes a chunk)
 constexpr long long kMaxAttnRows = 65535LL * 32; // M * Hq / Hkv: 32-row blocks on one grid axis
-
-bool aligned16(const void *p)
-{
-    return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
-}
-
-bool aligned4(const void *p)
-{
-    return (reinterpret_cast<uintptr_t>(p) & 3u) == 0;
-}
 
 // [a, a + n) and [b, b + m) (bytes) share a byte
 bool overlaps(const void *a, size_t n, const void *b, size_t m)
@@ -44,78 +39,11 @@ bi_status from_cuda(cudaError_t e)
     return e == cudaSuccess ? BI_OK : BI_ERR_CUDA;
 }
 
-// K range shared by every entry point.
-bi_status check_k(int K)
-{
-    if (K < 16 || (K % 16) != 0) return BI_ERR_INVALID_ARG;
-    if (static_cast<long long>(K) > kMaxK) return BI_ERR_INT32_BOUND;
-    return BI_OK;
-}
-
-// The library is built for sm_103a only.
-bi_status device_info(int *sm_count)
-{
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return BI_ERR_UNSUPPORTED;
-    int major = 0, minor = 0;
-    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
-        return BI_ERR_UNSUPPORTED;
-    if (major != 10 || minor != 3) return BI_ERR_UNSUPPORTED;
-    if (sm_count) {
-        if (cudaDeviceGetAttribute(sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-            return BI_ERR_UNSUPPORTED;
-    }
-    return BI_OK;
-}
-
-// cuTensorMapEncodeTiled through the runtime's driver entry point, so the
-// library does not link libcuda directly.
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn()
-{
-    static EncodeTiledFn fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-    });
-    return fn;
-}
-
-// 2-D int8 tensor [rows, cols] (row stride cols bytes), box box_cols x box_rows,
-// 128-byte swizzle, zero fill outside the tensor.
-bi_status encode_int8_2d(CUtensorMap *map, const void *base, long long rows, long long cols, int box_cols,
-                         int box_rows, bool stream_once)
-{
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) return BI_ERR_UNSUPPORTED;
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols)};
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                    stream_once ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B : CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? BI_OK : BI_ERR_CUDA;
-}
-
 bi_status check_linear_args(const int8_t *q, const float *s_a, int M, int K, const int8_t *w_q, const float *s_w,
                             int N, void *ws, size_t ws_bytes)
 {
-    if (!q || !s_a || !w_q || !s_w) return BI_ERR_INVALID_ARG;
-    if (M < 1 || M > 65535 || N < 1) return BI_ERR_INVALID_ARG;
-    bi_status s = check_k(K);
+    const bi_status s = bi::host::check_linear_operands(q, s_a, M, K, w_q, s_w, N);
     if (s != BI_OK) return s;
-    if (!aligned16(q) || !aligned16(w_q) || !aligned4(s_a) || !aligned4(s_w)) return BI_ERR_ALIGNMENT;
     if (!ws || ws_bytes < bi::kWsBytes || !aligned16(ws)) return BI_ERR_WORKSPACE;
     return BI_OK;
 }
@@ -308,9 +236,16 @@ bi_status bi_greedy_verify(const int32_t *argmax, const int32_t *draft, int M, i
 
 bi_status bi_selftest_wait_timeout(void *ws, size_t ws_bytes, bi_stream_t stream)
 {
-    if (!ws || ws_bytes < bi::kWsBytes || !aligned4(ws)) return BI_ERR_WORKSPACE;
     const bi_status st = device_info(nullptr);
     if (st != BI_OK) return st;
+    if (!ws) {
+        // the no-alloc entry point's own scratch
+        int *word = nullptr;
+        const bi_status sw = bi::host::noalloc_status_word(&word);
+        if (sw != BI_OK) return sw;
+        return from_cuda(bi::launch_wait_selftest(word, stream));
+    }
+    if (ws_bytes < bi::kWsBytes || !aligned4(ws)) return BI_ERR_WORKSPACE;
     return from_cuda(bi::launch_wait_selftest(static_cast<int *>(ws), stream));
 }
 

@@ -50,3 +50,28 @@ def test_noalloc_rejects_more_tokens_than_the_scratch_holds(bi):
     sw = torch.ones(N, dtype=torch.float32, device=DEV)
     y = torch.zeros((M, N), dtype=torch.int16, device=DEV)
     assert _noalloc(bi, q, s, wq, sw, y) == bi.BI_ERR_UNSUPPORTED
+
+
+def test_noalloc_reports_a_timeout_through_its_scratch(bi):
+    """A bounded wait that gives up on the fixed scratch (the library's wait
+    self-test, pointed at the scratch) is reported once by
+    bi_linear_w8a8_noalloc_status, which restores the scratch: the status then
+    reads BI_OK again and the next two calls equal bi_linear_w8a8.  Nothing
+    faults or hangs."""
+    M, N, K = 5, 777, 2080
+    x = gen.act_bf16(5, 1, M, K, outliers=gen.outlier_channels(5, K), gain=20.0)
+    q, s = quant_act(bi, x)
+    wq, sw = weights(bi, gen.weight_f32(5, 1, 0, N, K), pow2=True)
+    ref = linear(bi, q, s, wq, sw)
+    stream = torch.cuda.current_stream().cuda_stream
+    y = torch.full((M, N), -1, dtype=torch.int16, device=DEV)
+    assert _noalloc(bi, q, s, wq, sw, y) == bi.BI_OK
+    assert bi.lib.bi_linear_w8a8_noalloc_status(stream) == bi.BI_OK
+    assert bi.lib.bi_selftest_wait_timeout(None, 0, stream) == bi.BI_OK
+    assert bi.lib.bi_linear_w8a8_noalloc_status(stream) == bi.BI_ERR_TIMEOUT
+    assert bi.lib.bi_linear_w8a8_noalloc_status(stream) == bi.BI_OK
+    for _ in range(2):
+        y.fill_(-1)
+        assert _noalloc(bi, q, s, wq, sw, y) == bi.BI_OK
+        assert bi.lib.bi_linear_w8a8_noalloc_status(stream) == bi.BI_OK
+        assert torch.equal(y, ref)
