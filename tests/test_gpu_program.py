@@ -186,3 +186,35 @@ def test_program_quantize_crafted_rows_match_oracle(bi):
     torch.cuda.synchronize()
     assert np.array_equal(to_np(q), q_o)
     assert np.array_equal(to_np(s).view(np.uint32), s_o.view(np.uint32))
+
+
+@pytest.mark.parametrize("M,K,N", [(3, 1040, 528), (8, 4096, 1008), (1, 272, 48)])
+def test_program_linear_on_external_codes(bi, M, K, N):
+    """A program whose first linear reads codes quantised outside it (so they
+    arrive as int8, including a K that ends inside a 256-byte unit), followed
+    by a quantisation and a linear that read the program's own codes: both
+    equal the single calls."""
+    x = gen.act_bf16(21 + M, 1, M, K, outliers=gen.outlier_channels(21, K), gain=20.0)
+    w1 = weights(bi, gen.weight_f32(21, 1, 0, N, K), pow2=True)
+    w2 = weights(bi, gen.weight_f32(21, 2, 0, 2 * N, N), pow2=False)
+    q0, s0 = quant_act(bi, x)
+    y1_ref = linear(bi, q0, s0, *w1)
+    q1_ref = torch.empty((M, N), dtype=torch.int8, device=DEV)
+    s1_ref = torch.empty(M, dtype=torch.float32, device=DEV)
+    bi.bi_quantize_act(y1_ref, q1_ref, s1_ref)
+    y2_ref = linear(bi, q1_ref, s1_ref, *w2)
+    y1 = torch.full((M, N), -1, dtype=torch.int16, device=DEV)
+    y2 = torch.full((M, 2 * N), -1, dtype=torch.int16, device=DEV)
+    q1 = torch.empty((M, N), dtype=torch.int8, device=DEV)
+    s1 = torch.empty(M, dtype=torch.float32, device=DEV)
+    ops = [bi.op_linear(q0, s0, *w1, y1), bi.op_quantize_act(y1, q1, s1), bi.op_linear(q1, s1, *w2, y2)]
+    prog = bi.new_program(len(ops))
+    bi.bi_program_build(ops, prog)
+    ws = torch.zeros(bi.bi_program_workspace_size(), dtype=torch.uint8, device=DEV)
+    for _ in range(2):
+        bi.bi_program_run(prog, M, ws)
+        torch.cuda.synchronize()
+        assert bi.bi_workspace_status(ws) == bi.BI_OK
+        assert torch.equal(y1, y1_ref)
+        assert torch.equal(q1, q1_ref) and torch.equal(s1, s1_ref)
+        assert torch.equal(y2, y2_ref)
