@@ -17,9 +17,12 @@ the GPU and stay resident; the step reads all of them, far more than the L2
 cache, so no explicit flush is needed.
 
 `value` is weight GB/s over the step (weight codes + scales / step time) with
-the step in a CUDA graph; `e2e` is the same metric with the step's input rows
-copied from pinned host memory and the argmax copied back inside the timed
-region.
+the step in a CUDA graph; `e2e` is the same metric measured on the host clock
+with, every step, the input rows copied from pinned host memory, the library
+call made through the C ABI, the argmax and verification result copied back
+and waited for.  `per_config` times the public calls alone on every
+configuration's shapes (one linear, each Qwen3-8B projection at M = 1..8, the
+LM head at M = 1..8).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--m M] [--mode program|calls]
     python bench.py --impl reference     # the CPU oracle on a bounded sample
@@ -76,6 +79,11 @@ def parse():
                    help="with --attn-only: comma-separated M:T0:copies cases (default: the four of the sweep)")
     p.add_argument("--mode", default="program", choices=["program", "calls"],
                    help="program: the step as one verify-pass program launch; calls: one launch per op")
+    p.add_argument("--per-config-only", action="store_true",
+                   help="time only the public calls on each configuration's shapes and print their figures")
+    p.add_argument("--linear-only", default="", metavar="NAME:M",
+                   help="time only one linear of the stack (q, k, v, o, gate, up, down, qkv, gu or head) at M "
+                        "tokens, through bi_linear_w8a8 (bi_lmhead_argmax for head), rotating over the layers")
     return p.parse_args()
 
 
@@ -314,6 +322,140 @@ class Stack:
     def linear_bytes(self, M):
         bi = self.bi
         return sum(self.op_bytes(o) for o in self.ops(M) if o.kind == bi.BI_OP_LINEAR)
+
+
+# The stack's projections as row slices of its packed weight groups:
+# name -> (group, first row, rows).  K is the group's.
+STACK_LINEARS = {"q": ("qkv", 0, 4096), "k": ("qkv", 4096, 1024), "v": ("qkv", 5120, 1024), "o": ("o", 0, 4096),
+                 "gate": ("gu", 0, 12288), "up": ("gu", 12288, 12288), "down": ("down", 0, 4096),
+                 "qkv": ("qkv", 0, 6144), "gu": ("gu", 0, 24576)}
+
+
+def linear_measure(bi, torch, st, stream, peaks, name, M, reps=3):
+    """One public call on one of the stack's shapes at M tokens, timed through
+    the C ABI: bi_linear_w8a8 for a projection (the weights of layer l for the
+    l-th call, so the matrices rotate over all the stack's layers, far more
+    than L2), bi_lmhead_argmax for the head (622 MB, more than L2 by itself).
+    A CUDA graph of the calls (programmatic dependent launch), timed with
+    events on the launching stream; returns microseconds per call and weight
+    GB/s."""
+    import gen
+    dev = st.dev
+    peak = float(peaks["hbm_gbs"])
+    if name == "head":
+        wq, sw = st.head
+        K, N, layers = wq.shape[1], wq.shape[0], [st.head]
+    else:
+        g, r0, n = STACK_LINEARS[name]
+        layers = [(W[g][0][r0:r0 + n], W[g][1][r0:r0 + n]) for W in st.W]
+        K, N = layers[0][0].shape[1], n
+    x = torch.from_numpy(gen.activations(gen.QWEN3_8B, M, K).view(np.int16)).to(dev)
+    q = torch.empty((M, K), dtype=torch.int8, device=dev)
+    s = torch.empty(M, dtype=torch.float32, device=dev)
+    bi.bi_quantize_act(x, q, s)
+    y = torch.empty((M, N), dtype=torch.int16, device=dev)
+    am = torch.empty(M, dtype=torch.int32, device=dev)
+    calls = max(len(layers) * reps, 12)
+
+    def enqueue():
+        for i in range(calls):
+            wq, sw = layers[i % len(layers)]
+            if name == "head":
+                bi.bi_lmhead_argmax(q, s, wq, sw, None, am, st.ws, flags=bi.BI_FLAG_PDL)
+            else:
+                bi.bi_linear_w8a8(q, s, wq, sw, y, st.ws, flags=bi.BI_FLAG_PDL)
+
+    with torch.cuda.stream(stream):
+        enqueue()
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        enqueue()
+    with torch.cuda.stream(stream):    # replays run on the current stream
+        for _ in range(3):
+            g.replay()
+    stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n_rep = 3
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(n_rep):
+            g.replay()
+        e1.record(stream)
+    stream.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / (n_rep * calls)
+    wbytes = N * K + 4 * N
+    gbs = wbytes / (us * 1e-6) / 1e9
+    return {"us": round(us, 2), "weight_gbs": round(gbs, 1), "frac_of_hbm_copy": round(gbs / peak, 4),
+            "N": N, "K": K, "weight_bytes": wbytes, "rotating_copies": len(layers)}
+
+
+def per_config_measure(bi, torch, st, stream, peaks):
+    """The public calls on the shapes of each workload configuration.
+
+    single_linear: M = 2, K = N = 1024 (L2-resident: a latency case), the
+    activation quantisation and the linear back to back in a CUDA graph.
+    qwen3_8b_linears: every projection of a Qwen3-8B layer (and the packed
+    q/k/v and gate/up groups the verify pass uses) at M in {1,2,3,4,5,8}.
+    lm_head: bi_lmhead_argmax over 151,936 rows at M = 1..8."""
+    import gen
+    dev = st.dev
+    out = {}
+    # single linear (its own weights: the recipe of that configuration)
+    wl = gen.SINGLE
+    M, K, N = 2, 1024, 1024
+    w = torch.from_numpy(gen.weight_f32(wl.seed, 0, 0, N, K)).to(dev)
+    wq = torch.empty((N, K), dtype=torch.int8, device=dev)
+    sw = torch.empty(N, dtype=torch.float32, device=dev)
+    bi.bi_quantize_weight(w, wq, sw)
+    bi.bi_requant_pow2(wq, sw, wq, sw)
+    x = torch.from_numpy(gen.activations(wl, M, K).view(np.int16)).to(dev)
+    q = torch.empty((M, K), dtype=torch.int8, device=dev)
+    s = torch.empty(M, dtype=torch.float32, device=dev)
+    y = torch.empty((M, N), dtype=torch.int16, device=dev)
+    reps = 200
+
+    def pair():
+        for _ in range(reps):
+            bi.bi_quantize_act(x, q, s, flags=bi.BI_FLAG_PDL)
+            bi.bi_linear_w8a8(q, s, wq, sw, y, st.ws, flags=bi.BI_FLAG_PDL)
+
+    def linear_alone():
+        for _ in range(reps):
+            bi.bi_linear_w8a8(q, s, wq, sw, y, st.ws, flags=bi.BI_FLAG_PDL)
+
+    single = {}
+    for key, fn in (("quantize_and_linear_us", pair), ("linear_us", linear_alone)):
+        with torch.cuda.stream(stream):
+            fn()
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        with torch.cuda.stream(stream):    # replays run on the current stream
+            g.replay()
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(5):
+                g.replay()
+            e1.record(stream)
+        stream.synchronize()
+        single[key] = round(e0.elapsed_time(e1) * 1e3 / (5 * reps), 2)
+    single["note"] = ("M=2, K=N=1024 (1 MB of weights: L2-resident), back to back in a CUDA graph with "
+                      "programmatic dependent launch; a latency figure, not a roofline one")
+    out["single_linear"] = single
+    # the Qwen3-8B projections
+    lins = {}
+    for name in ("q", "k", "v", "o", "gate", "up", "down", "qkv", "gu"):
+        lins[name] = {str(m): linear_measure(bi, torch, st, stream, peaks, name, m) for m in (1, 2, 3, 4, 5, 8)}
+    out["qwen3_8b_linears"] = lins
+    out["lm_head"] = {str(m): linear_measure(bi, torch, st, stream, peaks, "head", m) for m in range(1, 9)}
+    out["note"] = ("each call through the C ABI (bi_linear_w8a8 / bi_lmhead_argmax); projections are row "
+                   "slices of the stack's packed groups, layer l's weights for the l-th call (rotating over "
+                   "all layers, more than L2); weight_gbs = (N*K + 4N) bytes / time per call")
+    return out
 
 
 def prefill_measure(bi, torch, st, stream, peaks, Ms=(512, 2048)):
@@ -563,6 +705,18 @@ def run_ours(args):
             print(json.dumps({"prefill": prefill_measure(bi, torch, st, stream, peaks, Ms=(args.prefill_only,))}),
                   flush=True)
         return
+    if args.per_config_only:
+        peaks, _ = read_peaks()
+        if rank == 0:
+            print(json.dumps({"per_config": per_config_measure(bi, torch, st, stream, peaks)}), flush=True)
+        return
+    if args.linear_only:
+        peaks, _ = read_peaks()
+        name, m = args.linear_only.split(":")
+        if rank == 0:
+            print(json.dumps({"linear": {name: {m: linear_measure(bi, torch, st, stream, peaks, name, int(m))}}}),
+                  flush=True)
+        return
 
     def barrier():
         torch.cuda.synchronize()
@@ -651,25 +805,28 @@ def run_ours(args):
         note = ("achieved = algorithmic bytes (W + s_w + q + s_a + y) of the step's %d linear launches / "
                 "their event-timed duration back to back in a CUDA graph" % lin_launches)
 
-    # end to end: the input rows H2D from pinned memory, the step's graph, argmax D2H
+    # end to end through the public API, as a verify loop runs it: every step
+    # copies its input rows host->device from pinned memory, makes the library
+    # call (bi_program_run; in calls mode one call per op), copies the argmax
+    # and the verification result back, and waits for them on the host
     host_h0 = torch.from_numpy(st.h0_np.view(np.int16)).pin_memory()
     host_am = torch.empty(16, dtype=torch.int32).pin_memory()
     host_acc = torch.empty(2, dtype=torch.int32).pin_memory()
     h2d = int(host_h0[:M].numel()) * 2
     e2e_steps = max(3, args.steps // 2)
-    barrier()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(e2e_steps):
+        enqueue_step(M)
+    barrier()
+    t_e2e = time.perf_counter()
+    for _ in range(e2e_steps):
+        with torch.cuda.stream(stream):
             st.h0[:M].copy_(host_h0[:M], non_blocking=True)
-            g.replay()
+            enqueue_step(M)
             host_am[:M].copy_(st.argmax[:M], non_blocking=True)
             host_acc.copy_(st.accept, non_blocking=True)
-        e1.record(stream)
-    barrier()
-    e2e_ms = reduce_max(e0.elapsed_time(e1) / e2e_steps, world, dev)
+        stream.synchronize()
+    e2e_ms = (time.perf_counter() - t_e2e) * 1e3 / e2e_steps
+    e2e_ms = reduce_max(e2e_ms, world, dev)
     e2e_gbs = job_rate(st.weight_bytes, world, e2e_ms)
 
     peaks, kind = read_peaks()
@@ -680,6 +837,7 @@ def run_ours(args):
     if NCU_TRAFFIC["source_sha256"] == source_sha(src):
         traffic = NCU_TRAFFIC["bytes_per_launch"]
 
+    per_config = per_config_measure(bi, torch, st, stream, peaks) if not args.no_sweep else None
     prefill = prefill_measure(bi, torch, st, stream, peaks) if not args.no_sweep else None
     block_scaled = blockq_measure(bi, torch, dev, stream, peaks) if not args.no_sweep else None
     attention = attention_measure(bi, torch, dev, stream, peaks) if not args.no_sweep else None
@@ -713,10 +871,14 @@ def run_ours(args):
                          "launch_us": round(lin_ms * 1e3 / lin_launches, 3),
                          "peak_kind": kind, "note": note},
             "e2e": {"value": round(e2e_gbs, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": 4 * M + 8, "ms_per_step": round(e2e_ms, 4)},
+                    "d2h_bytes_per_step": 4 * M + 8, "ms_per_step": round(e2e_ms, 4),
+                    "how": ("host wall clock per step: H2D of the input rows from pinned memory, the "
+                            "library call through the C ABI (no graph), D2H of argmax and verification "
+                            "result, host waits for the result every step")},
             "gpu_launches": st.launches_per_step(args.mode) * args.steps,
             "clocks": clk,
             "cpu_baseline": cpu,
+            "per_config": per_config,
             "prefill": prefill,
             "block_scaled": block_scaled,
             "attention": attention,

@@ -364,7 +364,7 @@ BI_API bi_status bi_selftest_quotient(unsigned long long *out, bi_stream_t strea
  * activation, stream a weight matrix, ...).  Launched one call at a time each
  * step pays a launch, a ramp to full memory bandwidth and a tail, which for
  * the smaller projections cost more than the weight read itself.  A program
- * runs all of them in one cooperative launch (one CTA per SM): op i starts
+ * runs all of them in one cooperative launch (two CTAs per SM): op i starts
  * only after every op before it has completed on the whole GPU (a grid-wide
  * barrier), so an op may read anything earlier ops wrote, while the weight
  * tiles of the ops ahead keep streaming into shared memory across the
@@ -453,7 +453,7 @@ BI_API bi_status bi_program_run(const void *program, int max_tokens, void *ws, s
  * so that the next call is reliable again.  Allocates nothing.
  */
 #define BI_NOALLOC_MAX_M 16
-#define BI_NOALLOC_SCRATCH_BYTES 1082624
+#define BI_NOALLOC_SCRATCH_BYTES 2164992
 BI_API bi_status bi_linear_w8a8_noalloc(const int8_t *q, const float *s_a, int M, int K,
                                         const int8_t *w_q, const float *s_w, int N,
                                         uint16_t *y, unsigned flags, bi_stream_t stream);

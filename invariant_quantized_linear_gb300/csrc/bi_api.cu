@@ -69,7 +69,7 @@ bi_status run_skinny(const int8_t *q, const float *s_a, int M, int K, const int8
     a.K = K;
     a.ws = bi::workspace_view(ws);
     a.pdl = (flags & BI_FLAG_PDL) != 0;
-    a.grid = sms < kMaxGrid ? sms : kMaxGrid;
+    a.grid = bi::host::skinny_grid(sms, N, K, bi::kMaxGrid);
     return from_cuda(bi::launch_skinny(a, stream));
 }
 

@@ -23,7 +23,7 @@
 namespace {
 
 // The scratch: exactly the workspace layout of the weight-streaming kernel
-// (kWsBytes, about 1.03 MiB), shared by every call on a device.  Static device
+// (kWsBytes, about 2.1 MiB), shared by every call on a device.  Static device
 // memory starts zeroed, and the kernel leaves its counters and partial sums at
 // zero when it completes, so a call needs no clearing before it.
 static_assert(bi::kWsBytes == BI_NOALLOC_SCRATCH_BYTES, "documented scratch size");
@@ -115,7 +115,7 @@ extern "C" BI_API bi_status bi_linear_w8a8_noalloc(const int8_t *q, const float 
     a.K = K;
     a.ws = bi::workspace_view(scratch);
     a.pdl = (flags & BI_FLAG_PDL) != 0;
-    a.grid = sms < bi::kMaxGrid ? sms : bi::kMaxGrid;
+    a.grid = bi::host::skinny_grid(sms, N, K, bi::kMaxGrid);
     return bi::launch_skinny(a, stream) == cudaSuccess ? BI_OK : BI_ERR_CUDA;
 }
 

@@ -100,6 +100,16 @@ inline bi_status encode_int8_2d(CUtensorMap *map, const void *base, long long ro
     return r == CUDA_SUCCESS ? BI_OK : BI_ERR_CUDA;
 }
 
+// CTAs of the weight-streaming kernel: two per SM for a large weight matrix
+// (measured faster from about 50 MB up: more bytes in flight per SM), one per
+// SM for smaller ones (faster below about 25 MB: less fixed cost per CTA).
+inline int skinny_grid(int sms, int N, int K, int max_grid)
+{
+    const bool large = static_cast<long long>(N) * K >= (32LL << 20);
+    const int g = large ? 2 * sms : sms;
+    return g < max_grid ? g : max_grid;
+}
+
 // The status word of the no-alloc entry point's fixed scratch on the current
 // device (defined with that scratch, in bi_noalloc.cu).
 bi_status noalloc_status_word(int **out);

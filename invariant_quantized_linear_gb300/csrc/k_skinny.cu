@@ -4,9 +4,10 @@
 // The weight read is the whole cost of such a pass ("why speculative decoding
 // changed my output", Fig. 1; "My speculative decoder got slower", "The
 // physics"), so the kernel is built to stream W at HBM speed:
-//  * persistent grid, one CTA per SM; the flattened sequence of units
+//  * persistent grid, two CTAs per SM for a large matrix, one for a small
+//    one (the caller's choice, by measured speed); the flattened sequence of units
 //    (64 weight rows x 256 bytes of K) is cut into equal contiguous ranges,
-//    one per CTA, so every SM reads the same number of bytes;
+//    one per CTA, so every CTA reads the same number of bytes;
 //  * a producer warp moves each unit's weight tile and the matching slice of
 //    the int8 activations into a ring of shared-memory stages with TMA
 //    (128-byte swizzle, evict-first L2 policy for the weights);

@@ -18,7 +18,7 @@ namespace bi {
 // A slot is owned by the CTA in whose range a split row block starts, so at
 // most one split row block maps to a slot.  Counters and partials are reset
 // by the kernel that consumes them, so a zero-filled workspace stays zeroed.
-constexpr int kMaxGrid = 256;
+constexpr int kMaxGrid = 512;
 constexpr int kBM = 64;        // weight rows per row block (4 warps x 16)
 constexpr int kMaxTok = 16;    // token columns kept per partial row
 constexpr size_t kWsCtrlBytes = 256;

@@ -153,8 +153,9 @@ def test_workspace_left_zeroed(bi):
     # per-CTA argmax keys are scratch that is overwritten by every call; all
     # counters and partial sums must be back at zero
     from invariant_quantized_linear_gb300 import lib  # noqa: F401  (library loaded)
-    head = ws[:256 + 4 * 256]
-    part = ws[256 + 4 * 256 + 8 * 256 * 16:]
+    G = 512   # per-CTA slots of the workspace (up to two CTAs per SM)
+    head = ws[:256 + 4 * G]
+    part = ws[256 + 4 * G + 8 * G * 16:]
     assert int(head.count_nonzero()) == 0 and int(part.count_nonzero()) == 0
     assert bi.bi_workspace_status(ws) == bi.BI_OK
 
