@@ -384,6 +384,286 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_chunk_kernel(AttnArgs a)
     }
 }
 
+// The chunk kernel for a kv head with few rows (M * G <= R, R = 4 or 8: one
+// or two verify queries of a Qwen3-8B-shaped layer).  The 32-row tile above
+// would leave most of its lanes idle.  One CTA per (chunk, kv head), eight
+// warps:
+//   score warps 0-3: thread t holds positions t and t + 128 for all R rows
+//           (each q row pair, broadcast from shared memory, serves both
+//           positions).  Each warp stages the K rows of its own 64 positions
+//           and starts as soon as they have landed.
+//   staging warps 4-7: issue the V copies once the score warps' K has landed
+//           (so that V does not slow K down in the memory system; the wait
+//           is bounded and only orders the requests).
+//   values, all warps: warp w holds d pairs 32 (w % n) + lane (n = D / 64)
+//           of R n / 8 rows (at least one), one packed chain per row over
+//           positions in order (the lanes are d, d + 1) and the row's weight
+//           sum l beside it.  The weights are stored row by row, so that one
+//           16-byte broadcast brings four positions of a row.
+// Every sum is the same sequence of correctly rounded operations as in the
+// 32-row kernel.
+template <int D, int R>
+struct SmallSmem {
+    static constexpr int kRow = 2 * D + 16;            // bytes per K row (padded: conflict-free row reads)
+    static constexpr int kK = 0;                       // K [256][kRow]
+    static constexpr int kV = kK + kChunk * kRow;      // V [256][D] bf16
+    static constexpr int kQ = kV + kChunk * 2 * D;     // q fp32 [D][R]
+    static constexpr int kP = kQ + D * R * 4;          // weights fp32 [R][256]
+    static constexpr int kRed = kP + kChunk * R * 4;   // score-warp maxima fp32 [R][4]
+    static constexpr int kFlag = kRed + R * 4 * 4;     // score warps whose K has landed
+    static constexpr int kBytes = kFlag + 16;
+};
+
+constexpr int kSmallThreads = 256;
+constexpr int kScoreThreads = 128;                     // warps 0-3
+
+__device__ __forceinline__ void bar_sync_scorers() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+constexpr int kKWaitLimit = 4096;                      // polls of the K-landed count before V is issued anyway
+
+template <int D, int R>
+__global__ void __launch_bounds__(kSmallThreads, 1) attn_chunk_small_kernel(AttnArgs a)
+{
+    using L = SmallSmem<D, R>;
+    constexpr int kW = D / 8;                          // 16-byte pieces of a K, V or q row
+    constexpr int kDG = D / 64;                        // 32-lane groups of d pairs (1 or 2)
+    constexpr int kRPW = (R * kDG >= 8) ? R * kDG / 8 : 1;   // rows per value warp (1 or 2)
+    constexpr int kQPer = (R * kW + kScoreThreads - 1) / kScoreThreads;
+    static_assert((R == 4 || R == 8) && kSmallThreads == 256, "shape");
+    extern __shared__ __align__(16) unsigned char smem[];
+    unsigned char *Ks = smem + L::kK;
+    unsigned char *Vs = smem + L::kV;
+    float *Qs = reinterpret_cast<float *>(smem + L::kQ);
+    float *Ps = reinterpret_cast<float *>(smem + L::kP);
+    float *red = reinterpret_cast<float *>(smem + L::kRed);
+    int *k_landed = reinterpret_cast<int *>(smem + L::kFlag);
+
+    const int c = blockIdx.x, hk = blockIdx.y;
+    const int G = a.Hq / a.Hkv;
+    const int rows = a.M * G;                          // rows of this kv head, <= R
+    const int n_max = chunk_positions(a.T0, a.M - 1, c);
+    if (n_max == 0) return;
+    pdl_launch_dependents();                           // the merge may launch; it waits for this grid to end
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int t0 = kChunk * c;
+    const size_t kv_row = static_cast<size_t>(a.Hkv) * D;
+    const bool scorer = tid < kScoreThreads;
+    if (tid == 0) *k_landed = 0;
+    __syncthreads();
+    // positions of chunk c that row r's query sees (0 past the rows)
+    auto row_n = [&](int r) { return r < rows ? chunk_positions(a.T0, r / G, c) : 0; };
+
+    float s[2][R];                                     // scores of positions tid, tid + 128 (score warps)
+    if (scorer) {
+        // q pieces (row i % R, 16-byte piece i / R), then the K rows of this
+        // warp's positions 32 w .. + 31 and 128 + 32 w .. + 31
+        uint4 qv[kQPer];
+#pragma unroll
+        for (int k = 0; k < kQPer; ++k) {
+            const int i = tid + k * kScoreThreads, qr = i % R;
+            qv[k] = make_uint4(0u, 0u, 0u, 0u);
+            if (i < R * kW && qr < rows) {
+                const int m = qr / G, h = hk * G + (qr - m * G);
+                qv[k] = __ldg(reinterpret_cast<const uint4 *>(a.q + (static_cast<size_t>(m) * a.Hq + h) * D) + i / R);
+            }
+        }
+        for (int i = lane; i < 64 * kW; i += 32) {
+            const int j = i / kW, sg = i - j * kW;
+            const int t = (j < 32) ? 32 * warp + j : 128 + 32 * warp + (j - 32);
+            if (t < n_max) cp_async16(Ks + t * L::kRow + 16 * sg, a.k + (t0 + t) * kv_row + hk * D + 8 * sg);
+        }
+        cp_async_commit();
+#pragma unroll
+        for (int k = 0; k < kQPer; ++k) {
+            const int i = tid + k * kScoreThreads, qr = i % R, qs = i / R;
+            if (i < R * kW) {
+                float *dst = Qs + 8 * qs * R + qr;     // q as [d][row]: a row pair is one 64-bit word
+                const uint32_t w[4] = {qv[k].x, qv[k].y, qv[k].z, qv[k].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    dst[(2 * e) * R] = __uint_as_float(w[e] << 16);
+                    dst[(2 * e + 1) * R] = __uint_as_float(w[e] & 0xFFFF0000u);
+                }
+            }
+        }
+        bar_sync_scorers();                            // q staged
+        cp_async_wait<0>();                            // this lane's K copies have landed
+        __syncwarp();                                  // and the other lanes' of the warp
+        if (lane == 0) atomicAdd(k_landed, 1);
+
+        // scores: R / 2 packed chains over d for each of the two positions
+        unsigned long long sc[2][R / 2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int ip = 0; ip < R / 2; ++ip) sc[h][ip] = 0ull;
+        const unsigned char *kb0 = Ks + tid * L::kRow;
+        const unsigned char *kb1 = Ks + (tid + 128) * L::kRow;
+        // fully unrolled with 4 rows of 128 (measured faster); otherwise by
+        // two pieces (a full unroll runs out of registers)
+#pragma unroll (R == 4 && D == 128 ? kW : 2)
+        for (int j = 0; j < kW; ++j) {
+            const uint4 k0 = *reinterpret_cast<const uint4 *>(kb0 + 16 * j);
+            const uint4 k1 = *reinterpret_cast<const uint4 *>(kb1 + 16 * j);
+            const uint32_t w0[4] = {k0.x, k0.y, k0.z, k0.w};
+            const uint32_t w1[4] = {k1.x, k1.y, k1.z, k1.w};
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int d = 8 * j + e;
+                unsigned long long q2[R / 2];
+#pragma unroll
+                for (int ip = 0; ip < R / 2; ip += 2) lds2x64(Qs + d * R + 2 * ip, q2[ip], q2[ip + 1]);
+                const float kf0 = __uint_as_float((e & 1) ? (w0[e >> 1] & 0xFFFF0000u) : (w0[e >> 1] << 16));
+                const float kf1 = __uint_as_float((e & 1) ? (w1[e >> 1] & 0xFFFF0000u) : (w1[e >> 1] << 16));
+                const unsigned long long kd0 = pk(kf0, kf0), kd1 = pk(kf1, kf1);
+#pragma unroll
+                for (int ip = 0; ip < R / 2; ++ip) {
+                    sc[0][ip] = fma2(q2[ip], kd0, sc[0][ip]);
+                    sc[1][ip] = fma2(q2[ip], kd1, sc[1][ip]);
+                }
+            }
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int ip = 0; ip < R / 2; ++ip) upk(sc[h][ip], s[h][2 * ip], s[h][2 * ip + 1]);
+        // scale, mask to the positions each row's query sees, maxima over the warp's 64 positions
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const int n = row_n(r);
+            s[0][r] = tid < n ? __fmul_rn(s[0][r], a.scale) : -INFINITY;
+            s[1][r] = tid + 128 < n ? __fmul_rn(s[1][r], a.scale) : -INFINITY;
+            float mx = fmaxf(s[0][r], s[1][r]);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            if (lane == 0) red[r * 4 + warp] = mx;
+        }
+    } else {
+        if (lane == 0) {
+            for (int it = 0; it < kKWaitLimit; ++it) {
+                if (*static_cast<volatile int *>(k_landed) >= kScoreThreads / 32) break;
+                __nanosleep(64);
+            }
+        }
+        __syncwarp();
+        for (int i = tid - kScoreThreads; i < n_max * kW; i += kSmallThreads - kScoreThreads) {
+            const int t = i / kW, sg = i - t * kW;
+            cp_async16(Vs + t * 2 * D + 16 * sg, a.v + (t0 + t) * kv_row + hk * D + 8 * sg);
+        }
+        cp_async_commit();
+    }
+    const ExpCoef ec = exp_coef();
+    __syncthreads();                                   // maxima of every row in red
+    if (scorer) {
+        // weights p = e(s - mx) into P[row][position]; masked positions weigh 0
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const float4 m4 = *reinterpret_cast<const float4 *>(red + r * 4);
+            const float mx = fmaxf(fmaxf(m4.x, m4.y), fmaxf(m4.z, m4.w));
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+                Ps[r * kChunk + tid + 128 * h] = s[h][r] == -INFINITY ? 0.0f : attn_e(__fsub_rn(s[h][r], mx), ec);
+        }
+    } else {
+        cp_async_wait<0>();                            // this thread's V copies have landed
+    }
+    __syncthreads();                                   // weights complete, V staged
+
+    // ---- weighted values and weight sums, positions in order
+    const int g = warp % kDG, rb = warp / kDG;         // d-pair group, row block
+    const int dp = 32 * g + lane;
+    const int r0 = kRPW * rb;                          // first row of this warp
+    if (r0 >= R) return;                               // D = 64 with 4 rows: half the warps have none
+    int nr[kRPW];
+    int n_lo = kChunk, n_hi = 0;
+#pragma unroll
+    for (int i = 0; i < kRPW; ++i) {
+        nr[i] = row_n(r0 + i);
+        if (nr[i] > 0) n_lo = min(n_lo, nr[i]);
+        n_hi = max(n_hi, nr[i]);
+    }
+    if (n_hi == 0) n_lo = 0;
+    unsigned long long acc[kRPW];                      // lanes d = 2 dp, 2 dp + 1 of row r0 + i
+    float lsum[kRPW];
+#pragma unroll
+    for (int i = 0; i < kRPW; ++i) {
+        acc[i] = 0ull;
+        lsum[i] = 0.0f;
+    }
+    const unsigned char *vb = Vs + 4 * dp;
+    const float *pb = Ps + r0 * kChunk;
+    // blocks of 4 positions: each row's 4 weights in one broadcast, the next
+    // block's operands in flight; rows with no positions have zero weights
+    // and are not written
+    uint32_t vq[4];
+    float4 pq[kRPW];
+    auto load4 = [&](int t, uint32_t (&vv)[4], float4 (&pp)[kRPW]) {
+        const int tt = min(t, kChunk - 4);             // past the chunk at the end: loaded, unused
+#pragma unroll
+        for (int k = 0; k < 4; ++k) vv[k] = *reinterpret_cast<const uint32_t *>(vb + (tt + k) * 2 * D);
+#pragma unroll
+        for (int i = 0; i < kRPW; ++i) pp[i] = *reinterpret_cast<const float4 *>(pb + i * kChunk + tt);
+    };
+    const int n_main = n_lo & ~3;
+    if (n_main > 0) load4(0, vq, pq);
+    for (int t = 0; t < n_main; t += 4) {
+        uint32_t vn[4];
+        float4 pn[kRPW];
+        load4(t + 4, vn, pn);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const unsigned long long v2 = pk(__uint_as_float(vq[k] << 16), __uint_as_float(vq[k] & 0xFFFF0000u));
+#pragma unroll
+            for (int i = 0; i < kRPW; ++i) {
+                const float p = k == 0 ? pq[i].x : k == 1 ? pq[i].y : k == 2 ? pq[i].z : pq[i].w;
+                acc[i] = fma2(pk(p, p), v2, acc[i]);
+                lsum[i] = __fadd_rn(lsum[i], p);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) vq[k] = vn[k];
+#pragma unroll
+        for (int i = 0; i < kRPW; ++i) pq[i] = pn[i];
+    }
+    // the last positions of the shortest row, then those only later queries see
+#pragma unroll 1
+    for (int t = n_main; t < n_hi; ++t) {
+        const uint32_t vv = *reinterpret_cast<const uint32_t *>(vb + t * 2 * D);
+        const unsigned long long v2 = pk(__uint_as_float(vv << 16), __uint_as_float(vv & 0xFFFF0000u));
+#pragma unroll
+        for (int i = 0; i < kRPW; ++i) {
+            if (t < nr[i]) {
+                const float p = pb[i * kChunk + t];
+                acc[i] = fma2(pk(p, p), v2, acc[i]);
+                lsum[i] = __fadd_rn(lsum[i], p);
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < kRPW; ++i) {
+        const int r = r0 + i;
+        if (nr[i] == 0) continue;                      // past the rows or past this query's positions
+        const int m = r / G, h = hk * G + (r - m * G);
+        float a0, a1;
+        upk(acc[i], a0, a1);
+        const float l = lsum[i];
+        if (a.T0 + m + 1 <= kChunk) {                  // the query's only chunk: o = a / l
+            const uint32_t ob = __bfloat16_as_ushort(__float2bfloat16_rn(__fdiv_rn(a0, l))) |
+                                (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(__fdiv_rn(a1, l))))
+                                 << 16);
+            *reinterpret_cast<uint32_t *>(a.o + (static_cast<size_t>(m) * a.Hq + h) * D + 2 * dp) = ob;
+        } else {
+            float *part = a.ws + ((static_cast<size_t>(m) * a.Hq + h) * a.Cmax + c) * (D + 4);
+            if (dp == 0) {
+                const float4 m4 = *reinterpret_cast<const float4 *>(red + r * 4);
+                part[0] = fmaxf(fmaxf(m4.x, m4.y), fmaxf(m4.z, m4.w));
+                part[1] = l;
+            }
+            *reinterpret_cast<float2 *>(part + 4 + 2 * dp) = make_float2(a0, a1);
+        }
+    }
+}
+
 // One CTA per (q head, query) whose query sees more than one chunk; thread d
 // makes o_d from the chunk results in chunk order.  The chunk weights w_c and
 // sums l_c are staged in shared memory first (their loads all in flight at
@@ -439,9 +719,29 @@ __global__ void __launch_bounds__(D) attn_merge_kernel(AttnArgs a)
     a.o[(static_cast<size_t>(m) * a.Hq + h) * D + d] = __bfloat16_as_ushort(__float2bfloat16_rn(__fdiv_rn(num, L)));
 }
 
-template <int D>
-cudaError_t launch_d(const AttnArgs &a, cudaStream_t stream)
+template <int D, int R>
+cudaError_t launch_small(const AttnArgs &a, cudaStream_t stream)
 {
+    constexpr int bytes = SmallSmem<D, R>::kBytes;
+    static bool configured = false;                    // one attribute call per process and shape
+    if (!configured) {
+        cudaError_t e =
+            cudaFuncSetAttribute(attn_chunk_small_kernel<D, R>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    attn_chunk_small_kernel<D, R>
+        <<<dim3(static_cast<unsigned>(a.Cmax), static_cast<unsigned>(a.Hkv)), kSmallThreads, bytes, stream>>>(a);
+    return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_rows(const AttnArgs &a, cudaStream_t stream)
+{
+    const int G = a.Hq / a.Hkv;
+    const int rows = a.M * G;
+    if (rows <= 4) return launch_small<D, 4>(a, stream);
+    if (rows <= 8) return launch_small<D, 8>(a, stream);
     constexpr int bytes = ChunkSmem<D>::kBytes;
     static bool configured = false;                    // one attribute call per process and head size
     if (!configured) {
@@ -449,12 +749,17 @@ cudaError_t launch_d(const AttnArgs &a, cudaStream_t stream)
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    const int G = a.Hq / a.Hkv;
-    const int blocks = (a.M * G + kRows - 1) / kRows;
+    const int blocks = (rows + kRows - 1) / kRows;
     attn_chunk_kernel<D><<<dim3(static_cast<unsigned>(a.Cmax), static_cast<unsigned>(a.Hkv),
                                 static_cast<unsigned>(blocks)),
                            kAttnThreads, bytes, stream>>>(a);
-    cudaError_t e = cudaGetLastError();
+    return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_d(const AttnArgs &a, cudaStream_t stream)
+{
+    cudaError_t e = launch_rows<D>(a, stream);
     if (e != cudaSuccess || a.Cmax == 1) return e;
     // the merge launches while the chunk grid runs (programmatic dependent
     // launch) and waits for it on the device

@@ -102,11 +102,13 @@ def test_later_queries_start_later(bi):
         _assert_same(_attn_gpu(bi, q[m:], k, v, T0 + m, scale), o[m:])
 
 
-def test_full_size_verify_attention(bi):
+@pytest.mark.parametrize("M", [8, 4, 3, 2, 1])
+def test_full_size_verify_attention(bi, M):
     """A Qwen3-8B-shaped layer's verify attention (32 query heads over 8 kv heads
-    of 128), M = 8 queries after 4096 cached positions: every output equals the
-    oracle's."""
-    M, Hq, Hkv, D, T0 = 8, 32, 8, 128, 4096
+    of 128), M queries after 4096 cached positions: every output equals the
+    oracle's.  M = 1 .. 4 run the small-row chunk kernel (4, 8 and 16 rows per
+    kv head), M = 8 the 32-row one."""
+    Hq, Hkv, D, T0 = 32, 8, 128, 4096
     q, k, v = gen.attn_qkv(5, M, Hq, Hkv, D, T0 + M)
     scale = 1.0 / math.sqrt(D)
     _assert_same(_attn_gpu(bi, q, k, v, T0, scale), oracle.attention(q, k, v, T0, scale))
