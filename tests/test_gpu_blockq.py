@@ -80,8 +80,11 @@ def test_activation_blocks_match_oracle(bi, M, K):
     assert np.array_equal(_np(d_a), d_o)
 
 
+# every token tile of the kernel (M = 1, 2-4, 5-8, 9-16), with 72 blocks per row
+# (lanes with three and with two blocks), 8 blocks (most lanes empty) and 256
+# or 384 blocks
 SHAPES = [(1, 1, 256), (2, 17, 512), (5, 100, 4096), (8, 1000, 4096), (16, 333, 1024), (3, 64, 12288),
-          (9, 31, 2304)]
+          (9, 31, 2304), (8, 40, 256), (6, 77, 12288), (12, 129, 8192), (16, 20, 12288)]
 
 
 @pytest.mark.parametrize("M,N,K", SHAPES)
