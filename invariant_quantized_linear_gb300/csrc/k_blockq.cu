@@ -149,11 +149,32 @@ __device__ __forceinline__ BlockW load_block(const uint8_t *__restrict__ ql, con
     return w;
 }
 
+__device__ __forceinline__ void q6_cp_async_16(void *smem, const void *gmem)
+{
+    const uint32_t sa = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(sa), "l"(gmem) : "memory");
+}
+
+__device__ __forceinline__ void q6_cp_async_4(void *smem, const void *gmem)
+{
+    const uint32_t sa = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(sa), "l"(gmem) : "memory");
+}
+
+// Shared-memory bytes of the staged activations of M tokens: per (token,
+// block) the 32 codes, the two sub-block sums and the scale.
+__host__ __device__ constexpr size_t q6_stage_bytes(int M, int K) { return static_cast<size_t>(M) * (K / 32) * 44; }
+
 // y [M, N] fp32, M <= MT.  One warp per R rows; lane l takes 32-blocks
 // l, l + 32, ... in that order (the next one's weights are loaded while the
 // current one is computed), and each activation block is loaded once for the
 // warp's R rows.  MT and R change the work per thread, not the adds.
-template <int MT, int R>
+// STAGED: the CTA first copies the activation codes and scales into shared
+// memory and forms each block's two sub-block sums once (instead of every
+// warp loading them from L1 and summing them per block); the block's two
+// 16-byte halves are stored swapped when bit 2 of its index is set, so that
+// 8 lanes reading 8 consecutive blocks hit distinct banks.
+template <int MT, int R, bool STAGED>
 __device__ __forceinline__ void linear_q6_body(const int8_t *__restrict__ qa, const float *__restrict__ d_a, int M,
                                                int K, const uint8_t *__restrict__ ql, const uint8_t *__restrict__ qh,
                                                const int8_t *__restrict__ sc, const float *__restrict__ d, int N,
@@ -165,8 +186,42 @@ __device__ __forceinline__ void linear_q6_body(const int8_t *__restrict__ qa, co
     }
     const int lane = threadIdx.x & 31;
     const int n0 = (blockIdx.x * kLinWarps + (threadIdx.x >> 5)) * R;
-    if (n0 >= N) return;
     const int nb = K / 32;
+    extern __shared__ __align__(16) unsigned char q6s[];
+    unsigned char *sact = q6s;                                                             // [M][nb][32]
+    int2 *ssum = reinterpret_cast<int2 *>(q6s + static_cast<size_t>(M) * nb * 32);         // [M][nb]
+    float *sda = reinterpret_cast<float *>(q6s + static_cast<size_t>(M) * nb * 40);       // [M][nb]
+    if constexpr (STAGED) {
+        const int items = M * nb;
+        for (int i = threadIdx.x; i < items; i += blockDim.x) {
+            const int b = i % nb;
+            const int8_t *src = qa + static_cast<size_t>(i / nb) * K + 32 * b;
+            unsigned char *dst = sact + static_cast<size_t>(i) * 32;
+            const int sw = (b >> 2) & 1;
+            q6_cp_async_16(dst + 16 * sw, src);
+            q6_cp_async_16(dst + 16 * (sw ^ 1), src + 16);
+            q6_cp_async_4(sda + i, d_a + i);
+        }
+        asm volatile("cp.async.commit_group;\n" ::: "memory");
+        asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+        for (int i = threadIdx.x; i < items; i += blockDim.x) {   // the items this thread copied
+            const int sw = ((i % nb) >> 2) & 1;
+            const uint4 h0 = *reinterpret_cast<const uint4 *>(sact + static_cast<size_t>(i) * 32 + 16 * sw);
+            const uint4 h1 = *reinterpret_cast<const uint4 *>(sact + static_cast<size_t>(i) * 32 + 16 * (sw ^ 1));
+            int s0 = 0, s1 = 0;
+            s0 = __dp4a(0x01010101, static_cast<int>(h0.x), s0);
+            s0 = __dp4a(0x01010101, static_cast<int>(h0.y), s0);
+            s0 = __dp4a(0x01010101, static_cast<int>(h0.z), s0);
+            s0 = __dp4a(0x01010101, static_cast<int>(h0.w), s0);
+            s1 = __dp4a(0x01010101, static_cast<int>(h1.x), s1);
+            s1 = __dp4a(0x01010101, static_cast<int>(h1.y), s1);
+            s1 = __dp4a(0x01010101, static_cast<int>(h1.z), s1);
+            s1 = __dp4a(0x01010101, static_cast<int>(h1.w), s1);
+            ssum[i] = make_int2(s0, s1);
+        }
+        __syncthreads();
+    }
+    if (n0 >= N) return;
     float p[MT][R];
 #pragma unroll
     for (int m = 0; m < MT; ++m)
@@ -188,19 +243,34 @@ __device__ __forceinline__ void linear_q6_body(const int8_t *__restrict__ qa, co
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
             if (m >= M) break;
-            const uint4 a0 = __ldg(reinterpret_cast<const uint4 *>(qa + static_cast<size_t>(m) * K) + 2 * b);
-            const uint4 a1 = __ldg(reinterpret_cast<const uint4 *>(qa + static_cast<size_t>(m) * K) + 2 * b + 1);
-            const float da = __ldg(d_a + static_cast<size_t>(m) * nb + b);
+            uint4 a0, a1;
+            float da;
+            int as0 = 0, as1 = 0;                      // sum(c a) = sum(u a) - 32 sum(a) per sub-block of 16
+            if constexpr (STAGED) {
+                const size_t it = static_cast<size_t>(m) * nb + b;
+                const int sw = (b >> 2) & 1;
+                a0 = *reinterpret_cast<const uint4 *>(sact + it * 32 + 16 * sw);
+                a1 = *reinterpret_cast<const uint4 *>(sact + it * 32 + 16 * (sw ^ 1));
+                da = sda[it];
+                const int2 as = ssum[it];
+                as0 = as.x;
+                as1 = as.y;
+            } else {
+                a0 = __ldg(reinterpret_cast<const uint4 *>(qa + static_cast<size_t>(m) * K) + 2 * b);
+                a1 = __ldg(reinterpret_cast<const uint4 *>(qa + static_cast<size_t>(m) * K) + 2 * b + 1);
+                da = __ldg(d_a + static_cast<size_t>(m) * nb + b);
+                as0 = __dp4a(0x01010101, static_cast<int>(a0.x), as0);
+                as0 = __dp4a(0x01010101, static_cast<int>(a0.y), as0);
+                as0 = __dp4a(0x01010101, static_cast<int>(a0.z), as0);
+                as0 = __dp4a(0x01010101, static_cast<int>(a0.w), as0);
+                as1 = __dp4a(0x01010101, static_cast<int>(a1.x), as1);
+                as1 = __dp4a(0x01010101, static_cast<int>(a1.y), as1);
+                as1 = __dp4a(0x01010101, static_cast<int>(a1.z), as1);
+                as1 = __dp4a(0x01010101, static_cast<int>(a1.w), as1);
+            }
             const int a[8] = {static_cast<int>(a0.x), static_cast<int>(a0.y), static_cast<int>(a0.z),
                               static_cast<int>(a0.w), static_cast<int>(a1.x), static_cast<int>(a1.y),
                               static_cast<int>(a1.z), static_cast<int>(a1.w)};
-            // sum(c a) = sum(u a) - 32 sum(a) per sub-block of 16: the same integer
-            int as0 = 0, as1 = 0;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                as0 = __dp4a(0x01010101, a[k], as0);
-                as1 = __dp4a(0x01010101, a[4 + k], as1);
-            }
 #pragma unroll
             for (int r = 0; r < R; ++r) {
                 int s0 = 0, s1 = 0;
@@ -230,7 +300,7 @@ __device__ __forceinline__ void linear_q6_body(const int8_t *__restrict__ qa, co
     }
 }
 
-template <int MT, int R>
+template <int MT, int R, bool STAGED>
 __global__ void __launch_bounds__(kLinWarps * 32) linear_q6_kernel(const int8_t *__restrict__ qa,
                                                                    const float *__restrict__ d_a, int M, int K,
                                                                    const uint8_t *__restrict__ ql,
@@ -239,7 +309,7 @@ __global__ void __launch_bounds__(kLinWarps * 32) linear_q6_kernel(const int8_t 
                                                                    const float *__restrict__ d, int N, float *y,
                                                                    int pdl)
 {
-    linear_q6_body<MT, R>(qa, d_a, M, K, ql, qh, sc, d, N, y, pdl);
+    linear_q6_body<MT, R, STAGED>(qa, d_a, M, K, ql, qh, sc, d, N, y, pdl);
 }
 
 // One token: fewer live registers, so more warps per SM keep weight loads in flight.
@@ -251,8 +321,10 @@ __global__ void __launch_bounds__(kLinWarps * 32, 5) linear_q6_kernel_m1(const i
                                                                          const float *__restrict__ d, int N, float *y,
                                                                          int pdl)
 {
-    linear_q6_body<1, 1>(qa, d_a, M, K, ql, qh, sc, d, N, y, pdl);
+    linear_q6_body<1, 1, false>(qa, d_a, M, K, ql, qh, sc, d, N, y, pdl);
 }
+
+constexpr size_t kQ6StageMax = 96 * 1024;
 
 template <int MT, int R>
 cudaError_t launch_q6(const int8_t *qa, const float *d_a, int M, int K, const uint8_t *ql, const uint8_t *qh,
@@ -268,10 +340,27 @@ cudaError_t launch_q6(const int8_t *qa, const float *d_a, int M, int K, const ui
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    if constexpr (MT == 1)
+    if constexpr (MT == 1) {
         return cudaLaunchKernelEx(&cfg, linear_q6_kernel_m1, qa, d_a, M, K, ql, qh, sc, d, N, y, pdl ? 1 : 0);
-    else
-        return cudaLaunchKernelEx(&cfg, linear_q6_kernel<MT, R>, qa, d_a, M, K, ql, qh, sc, d, N, y, pdl ? 1 : 0);
+    } else {
+        // the activations staged in shared memory while they fit beside a
+        // second CTA on the SM; otherwise loaded per warp
+        const size_t bytes = q6_stage_bytes(M, K);
+        if (bytes > kQ6StageMax)
+            return cudaLaunchKernelEx(&cfg, linear_q6_kernel<MT, R, false>, qa, d_a, M, K, ql, qh, sc, d, N, y,
+                                      pdl ? 1 : 0);
+        static bool configured = false;                // one attribute call per process and shape
+        if (!configured) {
+            const cudaError_t e = cudaFuncSetAttribute(linear_q6_kernel<MT, R, true>,
+                                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                       static_cast<int>(kQ6StageMax));
+            if (e != cudaSuccess) return e;
+            configured = true;
+        }
+        cfg.dynamicSmemBytes = bytes;
+        return cudaLaunchKernelEx(&cfg, linear_q6_kernel<MT, R, true>, qa, d_a, M, K, ql, qh, sc, d, N, y,
+                                  pdl ? 1 : 0);
+    }
 }
 
 }  // namespace
