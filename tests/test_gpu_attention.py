@@ -102,23 +102,24 @@ def test_later_queries_start_later(bi):
         _assert_same(_attn_gpu(bi, q[m:], k, v, T0 + m, scale), o[m:])
 
 
-@pytest.mark.parametrize("M", [8, 4, 3, 2, 1])
+@pytest.mark.parametrize("M", [16, 8, 4, 3, 2, 1])
 def test_full_size_verify_attention(bi, M):
     """A Qwen3-8B-shaped layer's verify attention (32 query heads over 8 kv heads
     of 128), M queries after 4096 cached positions: every output equals the
-    oracle's.  M = 1 .. 4 run the small-row chunk kernel (4, 8 and 16 rows per
-    kv head), M = 8 the 32-row one."""
+    oracle's.  M = 1, 2 run the small-row chunk kernel (4 and 8 rows per kv
+    head), M = 3 .. 8 the 32-row one, M = 16 two 32-row blocks per kv head."""
     Hq, Hkv, D, T0 = 32, 8, 128, 4096
     q, k, v = gen.attn_qkv(5, M, Hq, Hkv, D, T0 + M)
     scale = 1.0 / math.sqrt(D)
     _assert_same(_attn_gpu(bi, q, k, v, T0, scale), oracle.attention(q, k, v, T0, scale))
 
 
-def test_long_context_sampled_heads(bi):
+@pytest.mark.parametrize("M", [8, 4, 1])
+def test_long_context_sampled_heads(bi, M):
     """32768 cached positions (129 chunks): heads sampled across the kv groups,
     each compared with the oracle on that head alone (the heads of a group
     share a kv head, so a single-head oracle call on kv head h // 4 is exact)."""
-    M, Hq, Hkv, D, T0 = 4, 32, 8, 128, 32768
+    Hq, Hkv, D, T0 = 32, 8, 128, 32768
     q, k, v = gen.attn_qkv(19, M, Hq, Hkv, D, T0 + M)
     scale = 1.0 / math.sqrt(D)
     o = _attn_gpu(bi, q, k, v, T0, scale)

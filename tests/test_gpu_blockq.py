@@ -111,10 +111,12 @@ def test_rows_are_batch_invariant(bi):
         assert torch.equal(y.view(torch.int32), single[:M].view(torch.int32)), M
 
 
-def test_full_size_gate_up_sampled_rows(bi):
-    """gate/up of a Qwen3-8B layer (N = 24576, K = 4096) at M = 8, with PDL:
-    48 sampled output rows equal the oracle's."""
-    M, N, K = 8, 24576, 4096
+@pytest.mark.parametrize("M", [1, 8, 16])
+def test_full_size_gate_up_sampled_rows(bi, M):
+    """gate/up of a Qwen3-8B layer (N = 24576, K = 4096) at M = 1, 8 and 16 (the
+    sizes the benchmark times), with PDL: 48 sampled output rows equal the
+    oracle's."""
+    N, K = 24576, 4096
     w, x = _case(7, M, N, K)
     W = _weights_gpu(bi, w)
     q, d_a = _act_gpu(bi, x)
