@@ -52,6 +52,12 @@ SHAPES = [
     (16, 8, 1, 128, 4095, 1),     # sixteen queries over one kv head, 17 chunks
     (2, 6, 3, 128, 255, 0),       # the second query starts chunk 2 with one position
     (7, 16, 8, 64, 511, 5),       # 512 positions exactly for the first query
+    # at most 8 rows per kv head (the small-row chunk kernel)
+    (1, 4, 1, 64, 300, 2),        # 4 rows of 64: half the value warps have no row
+    (2, 8, 2, 64, 700, 0),        # 8 rows of 64 over three chunks
+    (2, 3, 1, 128, 260, 1),       # odd group: a row pair holds rows of two queries
+    (1, 8, 8, 128, 4095, 0),      # one row per kv head, the last chunk a single position
+    (2, 16, 4, 128, 1023, 3),     # 8 rows of 128, the second query starts a new chunk
 ]
 
 
