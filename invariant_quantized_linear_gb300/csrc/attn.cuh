@@ -14,6 +14,7 @@ struct AttnArgs {
     float *ws;           // [M, Hq, Cmax, D + 4] fp32 chunk results: mx, l, 2 unused, a[D]
     float scale;
     int M, Hq, Hkv, D, T0, Cmax;
+    int sms;             // the device's SM count (chooses between chunk kernels)
 };
 
 // Chunks of 256 positions the last query (which sees T0 + M positions) covers.

@@ -306,7 +306,8 @@ bi_status bi_attention_verify(const uint16_t *q, const uint16_t *k, const uint16
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return BI_ERR_ALIGNMENT;
     const size_t need = bi_attention_workspace_size(M, Hq, D, T0);
     if (need > 0 && (!ws || ws_bytes < need || !aligned16(ws))) return BI_ERR_WORKSPACE;
-    const bi_status st = device_info(nullptr);
+    int sms = 0;
+    const bi_status st = device_info(&sms);
     if (st != BI_OK) return st;
     bi::AttnArgs a;
     a.q = q;
@@ -321,6 +322,7 @@ bi_status bi_attention_verify(const uint16_t *q, const uint16_t *k, const uint16
     a.D = D;
     a.T0 = T0;
     a.Cmax = bi::attn_chunks(T0, M);
+    a.sms = sms;
     return from_cuda(bi::launch_attention(a, stream));
 }
 

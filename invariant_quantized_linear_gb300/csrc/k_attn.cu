@@ -664,6 +664,248 @@ __global__ void __launch_bounds__(kSmallThreads, 1) attn_chunk_small_kernel(Attn
     }
 }
 
+// ---- One or two queries with heads of 128: a cluster of four CTAs per (chunk,
+// kv head).  CTA k of the cluster stages a quarter of the chunk's K (positions
+// 64 k .. 64 k + 63) and a quarter of its V (d = 32 k .. 32 k + 31 of every
+// position), so each SM waits for a quarter of the bytes.  Row maxima and the
+// weights are exchanged through distributed shared memory:
+//   scores: thread (p, g) of warps 0-3 holds position 64 k + p for row pair g
+//           (two pairs with 8 rows), a packed chain over d in order;
+//   maxima: each CTA's row maxima go to every CTA of the cluster; barrier;
+//   weights: p = e(s - mx) of the CTA's 64 positions go to every CTA; barrier;
+//   values: thread (r, j) sums p_t v_td for d = 32 k + 2 j, + 1 of row r over
+//           all positions in order; warp 4 sums each row's weights l.
+// Every CTA of a cluster passes the same three cluster barriers: the only
+// early return comes before the first and is the same for the whole cluster
+// (it depends on the chunk alone), and the last remote store precedes the last
+// barrier.  The sums are the same correctly rounded steps as in the kernels
+// above.
+constexpr int kClusterCtas = 4;
+constexpr int kClusterThreads = 160;
+
+__device__ __forceinline__ uint32_t cluster_map(uint32_t local_smem, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_smem), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v)
+{
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+__device__ __forceinline__ void cluster_sync_all()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+template <int R>
+struct ClusterSmem {
+    static constexpr int kD = 128;
+    static constexpr int kRow = 2 * kD + 16;           // K row, padded
+    static constexpr int kK = 0;                       // K [64][kRow]: this CTA's positions
+    static constexpr int kV = kK + 64 * kRow;          // V [256][32] bf16: this CTA's d slice of every position
+    static constexpr int kQ = kV + kChunk * 64;        // q fp32 [128][R]
+    static constexpr int kP = kQ + kD * R * 4;         // weights fp32 [R][256] (every CTA's positions)
+    static constexpr int kRed = kP + R * kChunk * 4;   // row maxima fp32 [R][4 CTAs]
+    static constexpr int kWm = kRed + R * kClusterCtas * 4;   // warp maxima fp32 [4 warps][R]
+    static constexpr int kL = kWm + 4 * R * 4;         // weight sums fp32 [R]
+    static constexpr int kBytes = kL + R * 4;
+};
+
+template <int R>
+__global__ void __launch_bounds__(kClusterThreads) attn_chunk_cluster_kernel(AttnArgs a)
+{
+    constexpr int D = 128;
+    using L = ClusterSmem<R>;
+    constexpr int kW = D / 8;                          // 16-byte pieces of a q or K row
+    constexpr int kPairs = R / 2 / 2;                  // row pairs per score thread (1 or 2)
+    static_assert(R == 4 || R == 8, "shape");
+    extern __shared__ __align__(16) unsigned char smem[];
+    unsigned char *Ks = smem + L::kK;
+    unsigned char *Vs = smem + L::kV;
+    float *Qs = reinterpret_cast<float *>(smem + L::kQ);
+    float *Ps = reinterpret_cast<float *>(smem + L::kP);
+    float *red = reinterpret_cast<float *>(smem + L::kRed);
+    float *wm = reinterpret_cast<float *>(smem + L::kWm);
+    float *ls = reinterpret_cast<float *>(smem + L::kL);
+
+    const int k = blockIdx.x % kClusterCtas;          // rank in the cluster (clusters run along x)
+    const int c = blockIdx.x / kClusterCtas, hk = blockIdx.y;
+    const int G = a.Hq / a.Hkv;
+    const int rows = a.M * G;                          // <= R
+    const int n_max = chunk_positions(a.T0, a.M - 1, c);
+    if (n_max == 0) return;                            // the whole cluster: it depends on the chunk only
+    pdl_launch_dependents();
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int t0 = kChunk * c, tk = 64 * k;           // first position of the chunk, of this CTA's quarter
+    const size_t kv_row = static_cast<size_t>(a.Hkv) * D;
+    auto row_n = [&](int r) { return r < rows ? chunk_positions(a.T0, r / G, c) : 0; };
+
+    // ---- stage: q (all rows), K of this CTA's 64 positions, then V's d slice of all positions
+    for (int i = tid; i < 64 * kW; i += kClusterThreads) {
+        const int t = i / kW, sg = i - t * kW;
+        if (tk + t < n_max) cp_async16(Ks + t * L::kRow + 16 * sg, a.k + (t0 + tk + t) * kv_row + hk * D + 8 * sg);
+    }
+    cp_async_commit();
+    for (int i = tid; i < n_max * 4; i += kClusterThreads) {
+        const int t = i >> 2, sg = i & 3;
+        cp_async16(Vs + t * 64 + 16 * sg, a.v + (t0 + t) * kv_row + hk * D + 32 * k + 8 * sg);
+    }
+    cp_async_commit();
+    for (int i = tid; i < R * kW; i += kClusterThreads) {
+        const int qr = i % R, qs = i / R;
+        uint4 qv = make_uint4(0u, 0u, 0u, 0u);
+        if (qr < rows) {
+            const int m = qr / G, h = hk * G + (qr - m * G);
+            qv = __ldg(reinterpret_cast<const uint4 *>(a.q + (static_cast<size_t>(m) * a.Hq + h) * D) + qs);
+        }
+        float *dst = Qs + 8 * qs * R + qr;
+        const uint32_t w[4] = {qv.x, qv.y, qv.z, qv.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            dst[(2 * e) * R] = __uint_as_float(w[e] << 16);
+            dst[(2 * e + 1) * R] = __uint_as_float(w[e] & 0xFFFF0000u);
+        }
+    }
+    const ExpCoef ec = exp_coef();
+    cluster_sync_all();                                // 1: every CTA of the cluster is running
+    cp_async_wait<1>();                                // this thread's K copies have landed
+    __syncthreads();                                   // and everyone's; q staged
+
+    // ---- scores: warps 0-3, position p = tid % 64 of this quarter, row pairs g * kPairs ..
+    const bool scorer = tid < 128;
+    const int p = tid & 63, g = (tid >> 6) & 1;
+    float s[2 * kPairs];
+    if (scorer) {
+        unsigned long long sc[kPairs];
+#pragma unroll
+        for (int ip = 0; ip < kPairs; ++ip) sc[ip] = 0ull;
+        const unsigned char *kb = Ks + p * L::kRow;
+#pragma unroll 4
+        for (int j = 0; j < kW; ++j) {
+            const uint4 kj = *reinterpret_cast<const uint4 *>(kb + 16 * j);
+            const uint32_t w[4] = {kj.x, kj.y, kj.z, kj.w};
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int d = 8 * j + e;
+                const float kf = __uint_as_float((e & 1) ? (w[e >> 1] & 0xFFFF0000u) : (w[e >> 1] << 16));
+                const unsigned long long kd = pk(kf, kf);
+                if constexpr (kPairs == 2) {
+                    unsigned long long q2[2];
+                    lds2x64(Qs + d * R + 4 * g, q2[0], q2[1]);
+                    sc[0] = fma2(q2[0], kd, sc[0]);
+                    sc[1] = fma2(q2[1], kd, sc[1]);
+                } else {
+                    const unsigned long long q2 = *reinterpret_cast<const unsigned long long *>(Qs + d * R + 2 * g);
+                    sc[0] = fma2(q2, kd, sc[0]);
+                }
+            }
+        }
+#pragma unroll
+        for (int ip = 0; ip < kPairs; ++ip) upk(sc[ip], s[2 * ip], s[2 * ip + 1]);
+        // scale, mask, maxima over this warp's 32 positions
+#pragma unroll
+        for (int x = 0; x < 2 * kPairs; ++x) {
+            const int r = 2 * kPairs * g + x;
+            s[x] = tk + p < row_n(r) ? __fmul_rn(s[x], a.scale) : -INFINITY;
+            float mx = s[x];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            if (lane == 0) wm[warp * R + r] = mx;
+        }
+    }
+    __syncthreads();
+    // this CTA's maxima (over its 64 positions) to every CTA of the cluster
+    if (tid < R) {
+        const int r = tid, gw = r / (2 * kPairs);      // warps 2 gw, 2 gw + 1 hold row r
+        const float mx = fmaxf(wm[(2 * gw) * R + r], wm[(2 * gw + 1) * R + r]);
+        const uint32_t local = static_cast<uint32_t>(__cvta_generic_to_shared(red + r * kClusterCtas + k));
+#pragma unroll
+        for (int q = 0; q < kClusterCtas; ++q) st_cluster_f32(cluster_map(local, q), mx);
+    }
+    cluster_sync_all();                                // 2: every CTA has every quarter's maxima
+    // ---- weights of this quarter's positions to every CTA
+    if (scorer) {
+#pragma unroll
+        for (int x = 0; x < 2 * kPairs; ++x) {
+            const int r = 2 * kPairs * g + x;
+            const float4 m4 = *reinterpret_cast<const float4 *>(red + r * kClusterCtas);
+            const float mx = fmaxf(fmaxf(m4.x, m4.y), fmaxf(m4.z, m4.w));
+            const float pv = s[x] == -INFINITY ? 0.0f : attn_e(__fsub_rn(s[x], mx), ec);
+            const uint32_t local = static_cast<uint32_t>(__cvta_generic_to_shared(Ps + r * kChunk + tk + p));
+#pragma unroll
+            for (int q = 0; q < kClusterCtas; ++q) st_cluster_f32(cluster_map(local, q), pv);
+        }
+    }
+    cp_async_wait<0>();                                // this thread's V copies have landed
+    cluster_sync_all();                                // 3: all weights everywhere (the last remote stores)
+    __syncthreads();                                   // V staged by every thread
+
+    // ---- weight sums (warp 4) and weighted values (this CTA's d slice)
+    if (warp == 4) {
+        if (lane < R) {
+            const int r = lane, n = row_n(r);
+            const float *pr = Ps + r * kChunk;
+            float l = 0.0f;
+            int t = 0;
+            for (; t + 4 <= n; t += 4) {
+                const float4 p4 = *reinterpret_cast<const float4 *>(pr + t);
+                l = __fadd_rn(l, p4.x);
+                l = __fadd_rn(l, p4.y);
+                l = __fadd_rn(l, p4.z);
+                l = __fadd_rn(l, p4.w);
+            }
+            for (; t < n; ++t) l = __fadd_rn(l, pr[t]);
+            ls[r] = l;
+        }
+    }
+    const int r = tid >> 4, j = tid & 15;              // value unit: row r, d = 32 k + 2 j, + 1
+    const bool valuer = tid < 16 * R;
+    const int nr = valuer ? row_n(r) : 0;
+    unsigned long long acc = 0ull;
+    if (valuer && nr > 0) {
+        const float *pr = Ps + r * kChunk;
+        const unsigned char *vb = Vs + 4 * j;
+        int t = 0;
+        for (; t + 4 <= nr; t += 4) {
+            const float4 p4 = *reinterpret_cast<const float4 *>(pr + t);
+            const float pp[4] = {p4.x, p4.y, p4.z, p4.w};
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+                const uint32_t vv = *reinterpret_cast<const uint32_t *>(vb + (t + x) * 64);
+                acc = fma2(pk(pp[x], pp[x]), pk(__uint_as_float(vv << 16), __uint_as_float(vv & 0xFFFF0000u)), acc);
+            }
+        }
+        for (; t < nr; ++t) {
+            const float pv = pr[t];
+            const uint32_t vv = *reinterpret_cast<const uint32_t *>(vb + t * 64);
+            acc = fma2(pk(pv, pv), pk(__uint_as_float(vv << 16), __uint_as_float(vv & 0xFFFF0000u)), acc);
+        }
+    }
+    __syncthreads();                                   // the weight sums in ls
+    if (!valuer || nr == 0) return;
+    const int m = r / G, h = hk * G + (r - m * G);
+    float a0, a1;
+    upk(acc, a0, a1);
+    const float l = ls[r];
+    const int dd = 32 * k + 2 * j;
+    if (a.T0 + m + 1 <= kChunk) {                      // the query's only chunk: o = a / l
+        const uint32_t ob = __bfloat16_as_ushort(__float2bfloat16_rn(__fdiv_rn(a0, l))) |
+                            (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(__fdiv_rn(a1, l)))) << 16);
+        *reinterpret_cast<uint32_t *>(a.o + (static_cast<size_t>(m) * a.Hq + h) * D + dd) = ob;
+    } else {
+        float *part = a.ws + ((static_cast<size_t>(m) * a.Hq + h) * a.Cmax + c) * (D + 4);
+        if (k == 0 && j == 0) {
+            const float4 m4 = *reinterpret_cast<const float4 *>(red + r * kClusterCtas);
+            part[0] = fmaxf(fmaxf(m4.x, m4.y), fmaxf(m4.z, m4.w));
+            part[1] = l;
+        }
+        *reinterpret_cast<float2 *>(part + 4 + dd) = make_float2(a0, a1);
+    }
+}
+
 // One CTA per (q head, query) whose query sees more than one chunk; thread d
 // makes o_d from the chunk results in chunk order.  The chunk weights w_c and
 // sums l_c are staged in shared memory first (their loads all in flight at
@@ -735,11 +977,39 @@ cudaError_t launch_small(const AttnArgs &a, cudaStream_t stream)
     return cudaGetLastError();
 }
 
+template <int R>
+cudaError_t launch_cluster(const AttnArgs &a, cudaStream_t stream)
+{
+    constexpr int bytes = ClusterSmem<R>::kBytes;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(a.Cmax * kClusterCtas), static_cast<unsigned>(a.Hkv));
+    cfg.blockDim = dim3(kClusterThreads);
+    cfg.dynamicSmemBytes = bytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kClusterCtas;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, attn_chunk_cluster_kernel<R>, a);
+}
+
 template <int D>
 cudaError_t launch_rows(const AttnArgs &a, cudaStream_t stream)
 {
     const int G = a.Hq / a.Hkv;
     const int rows = a.M * G;
+    // the four-CTA clusters while they need at most two CTAs per SM (measured
+    // faster up to about 2048 cached positions at one and two queries); the
+    // one-CTA kernel on larger grids, where four CTAs sharing an SM cost more
+    // than the quarter-size staging saves
+    if constexpr (D == 128) {
+        const bool clusters = static_cast<long long>(a.Cmax) * a.Hkv * kClusterCtas <= 2LL * a.sms;
+        if (clusters && rows <= 4) return launch_cluster<4>(a, stream);
+        if (clusters && rows <= 8) return launch_cluster<8>(a, stream);
+    }
     if (rows <= 4) return launch_small<D, 4>(a, stream);
     if (rows <= 8) return launch_small<D, 8>(a, stream);
     constexpr int bytes = ChunkSmem<D>::kBytes;

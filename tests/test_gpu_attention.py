@@ -52,7 +52,8 @@ SHAPES = [
     (16, 8, 1, 128, 4095, 1),     # sixteen queries over one kv head, 17 chunks
     (2, 6, 3, 128, 255, 0),       # the second query starts chunk 2 with one position
     (7, 16, 8, 64, 511, 5),       # 512 positions exactly for the first query
-    # at most 8 rows per kv head (the small-row chunk kernel)
+    # at most 8 rows per kv head: heads of 128 on a grid of at most two CTAs
+    # per SM run the four-CTA cluster kernel, the rest the small-row kernel
     (1, 4, 1, 64, 300, 2),        # 4 rows of 64: half the value warps have no row
     (2, 8, 2, 64, 700, 0),        # 8 rows of 64 over three chunks
     (2, 3, 1, 128, 260, 1),       # odd group: a row pair holds rows of two queries
@@ -113,7 +114,8 @@ def test_full_size_verify_attention(bi, M):
     """A Qwen3-8B-shaped layer's verify attention (32 query heads over 8 kv heads
     of 128), M queries after 4096 cached positions: every output equals the
     oracle's.  M = 1, 2 run the small-row chunk kernel (4 and 8 rows per kv
-    head), M = 3 .. 8 the 32-row one, M = 16 two 32-row blocks per kv head."""
+    head; 17 chunks x 8 kv heads is too large a grid for the cluster kernel),
+    M = 3 .. 8 the 32-row one, M = 16 two 32-row blocks per kv head."""
     Hq, Hkv, D, T0 = 32, 8, 128, 4096
     q, k, v = gen.attn_qkv(5, M, Hq, Hkv, D, T0 + M)
     scale = 1.0 / math.sqrt(D)
