@@ -160,11 +160,15 @@ BI_API bi_status bi_requant_pow2(const int8_t *w_q, const float *s_w, int N, int
  * workspace holds split-K partial sums, their counters and a status word.  It
  * must be zero-filled before its first use (cudaMemset); every call that
  * completes leaves it zero-filled again, so one workspace can serve a whole
- * sequence of calls on one stream.  For M > 16 it is larger (about 12.6 MB):
- * it also holds the int32 partial sums of prefill tiles split along K to fill
- * the GPU's last wave (scratch: every call overwrites what it reads) and their
- * counters (zero between calls).  A workspace of the M <= 16 size still works
- * for M > 16, without that split (same results).
+ * sequence of calls on one stream.  For M > 16 it is larger: about 12.6 MB
+ * for the int32 partial sums of prefill tiles split along K to fill the GPU's
+ * last wave (scratch: every call overwrites what it reads) and their counters
+ * (zero between calls).  For M > 256 it also holds 2 * (M + N) * K bytes
+ * (each part rounded up to 256) for exact f16 copies of q and w_q that the
+ * tensor cores read by TMA (scratch).  A smaller workspace still works for
+ * M > 16, with the same results: without the f16 room the kernel converts
+ * the codes in its tile loop (slower above 256 tokens), and with only the
+ * M <= 16 size it also runs without the split.
  */
 BI_API size_t bi_linear_workspace_size(int M, int N, int K);
 

@@ -12,7 +12,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "libbi.so")
 BUILD = os.path.join(HERE, "_build")
-SOURCES = ["bi_api.cu", "k_quant.cu", "k_skinny.cu", "k_prefill.cu", "bi_noalloc.cu", "k_program.cu", "k_blockq.cu", "k_attn.cu", "k_probe.cu"]
+SOURCES = ["bi_api.cu", "k_quant.cu", "k_skinny.cu", "k_prefill.cu", "k_prefill_tma.cu", "bi_noalloc.cu", "k_program.cu", "k_blockq.cu", "k_attn.cu", "k_probe.cu"]
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",

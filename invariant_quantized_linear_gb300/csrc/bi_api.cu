@@ -173,9 +173,9 @@ bi_status bi_requant_pow2(const int8_t *w_q, const float *s_w, int N, int K, int
 
 size_t bi_linear_workspace_size(int M, int N, int K)
 {
-    (void)N;
-    (void)K;
-    return M > 16 ? bi::kWsPrefillBytes : bi::kWsBytes;
+    if (M <= 16) return bi::kWsBytes;
+    if (M <= bi::kPrefillTmaMinM || N < 1 || K < 1) return bi::kWsPrefillBytes;
+    return bi::kWsPrefillBytes + bi::prefill_f16_bytes(M, K) + bi::prefill_f16_bytes(N, K);
 }
 
 size_t bi_lmhead_workspace_size(int M, int N, int K)
@@ -196,13 +196,39 @@ bi_status bi_linear_w8a8(const int8_t *q, const float *s_a, int M, int K, const 
 
     st = device_info(nullptr);
     if (st != BI_OK) return st;
+    // a workspace sized for M <= 16 still works, without splitting tiles
+    const bool tail = ws_bytes >= bi::kWsPrefillBytes;
+    int32_t *tail_acc = tail ? reinterpret_cast<int32_t *>(static_cast<char *>(ws) + bi::kWsTailAccOff) : nullptr;
+    int *tail_cnt = tail ? reinterpret_cast<int *>(static_cast<char *>(ws) + bi::kWsTailCntOff) : nullptr;
+    if (M > bi::kPrefillTmaMinM && ws_bytes >= bi_linear_workspace_size(M, N, K)) {
+        // room for f16 copies of the operands: the TMA-fed kernel
+        bi::PrefillTmaArgs a;
+        char *f16 = static_cast<char *>(ws) + bi::kWsPrefillBytes;
+        a.q = q;
+        a.w_q = w_q;
+        a.qf = reinterpret_cast<uint16_t *>(f16);
+        a.wf = reinterpret_cast<uint16_t *>(f16 + bi::prefill_f16_bytes(M, K));
+        st = bi::host::encode_f16_2d(&a.map_a, a.qf, M, K, 64, 128);
+        if (st != BI_OK) return st;
+        st = bi::host::encode_f16_2d(&a.map_b, a.wf, N, K, 64, 256);
+        if (st != BI_OK) return st;
+        st = bi::host::encode_f16_2d(&a.map_bs, a.wf, N, K, 64, 32);
+        if (st != BI_OK) return st;
+        a.s_a = s_a;
+        a.s_w = s_w;
+        a.y = y;
+        a.M = M;
+        a.N = N;
+        a.K = K;
+        a.ws = bi::workspace_view(ws);
+        a.pdl = (flags & BI_FLAG_PDL) != 0;
+        return from_cuda(bi::launch_prefill_tma(a, stream));
+    }
     bi::PrefillArgs a;
     a.q = q;
     a.w_q = w_q;
-    // a workspace sized for M <= 16 still works, without splitting tiles
-    const bool tail = ws_bytes >= bi::kWsPrefillBytes;
-    a.tail_acc = tail ? reinterpret_cast<int32_t *>(static_cast<char *>(ws) + bi::kWsTailAccOff) : nullptr;
-    a.tail_cnt = tail ? reinterpret_cast<int *>(static_cast<char *>(ws) + bi::kWsTailCntOff) : nullptr;
+    a.tail_acc = tail_acc;
+    a.tail_cnt = tail_cnt;
     a.s_a = s_a;
     a.s_w = s_w;
     a.y = y;

@@ -100,6 +100,23 @@ inline bi_status encode_int8_2d(CUtensorMap *map, const void *base, long long ro
     return r == CUDA_SUCCESS ? BI_OK : BI_ERR_CUDA;
 }
 
+// 2-D f16 tensor [rows, cols] (row stride 2 * cols bytes), box box_cols x
+// box_rows, 128-byte swizzle, zero fill outside the tensor.
+inline bi_status encode_f16_2d(CUtensorMap *map, const void *base, long long rows, long long cols, int box_cols,
+                               int box_rows)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return BI_ERR_UNSUPPORTED;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(2 * cols)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? BI_OK : BI_ERR_CUDA;
+}
+
 // CTAs of the weight-streaming kernel: two per SM for a large weight matrix
 // (measured faster from about 50 MB up: more bytes in flight per SM), one per
 // SM for smaller ones (faster below about 25 MB: less fixed cost per CTA).

@@ -103,7 +103,39 @@ struct PrefillArgs {
     bool pdl;
 };
 
-// M > 16 tiled kernel (tcgen05).
+// M > 16 tiled kernel (tcgen05), converting the int8 operands in the tile loop.
 cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream);
+
+// Above kPrefillTmaMinM tokens, prefill workspaces also hold exact f16 copies
+// of the operands after kWsPrefillBytes: q [M, K], then w [N, K], each
+// 256-byte aligned (scratch: every call overwrites them before reading).  The
+// copies cost a pass over the weights (about 3 bytes per weight) whatever M
+// is; the TMA-fed kernel that reads them is faster than the converting one by
+// more than that above about 256 tokens (measured with N = 12288, K = 4096).
+constexpr int kPrefillTmaMinM = 256;
+inline size_t prefill_f16_bytes(long long rows, long long K)
+{
+    return static_cast<size_t>((rows * K * 2 + 255) / 256 * 256);
+}
+
+struct PrefillTmaArgs {
+    const int8_t *q;           // [M, K], rows 16-byte aligned
+    const int8_t *w_q;         // [N, K]
+    uint16_t *qf;              // [M, K] f16 copy (workspace)
+    uint16_t *wf;              // [N, K] f16 copy (workspace)
+    CUtensorMap map_a;         // qf: box 64 x 128, 128-byte swizzle
+    CUtensorMap map_b;         // wf: box 64 x 256, 128-byte swizzle
+    CUtensorMap map_bs;        // wf: box 64 x 32 (slices of the last wave's tiles)
+    const float *s_a;
+    const float *s_w;
+    uint16_t *y;
+    int M, N, K;
+    Workspace ws;
+    bool pdl;
+};
+
+// M > 16 tiled kernel (tcgen05) on f16 copies of the operands loaded by TMA,
+// after the pass that writes those copies.
+cudaError_t launch_prefill_tma(const PrefillTmaArgs &a, cudaStream_t stream);
 
 }  // namespace bi

@@ -45,13 +45,31 @@ PREFILL = [(17, 130, 256), (33, 257, 1024), (130, 300, 528), (200, 1000, 4096), 
            # exact fp32 chunks of 1024 K: a one-step last chunk, N tails on and
            # off the 16-byte store path, several token and weight tiles
            (129, 520, 1040), (300, 776, 3088)]
+# above 256 tokens the TMA-fed kernel runs (f16 copies in the workspace); its
+# last wave is cut into slices of 32 / 64 / 96 weight rows depending on how
+# many tiles it holds, and a ragged q copy ends in a partial 512-code block
+PREFILL_TMA = [(384, 300, 528), (400, 520, 1040), (520, 776, 3088), (257, 4096, 272), (1100, 2500, 1024)]
 
 
-@pytest.mark.parametrize("M,N,K", SKINNY + PREFILL)
+@pytest.mark.parametrize("M,N,K", SKINNY + PREFILL + PREFILL_TMA)
 @pytest.mark.parametrize("pow2", [True, False])
 def test_linear_matches_oracle(bi, M, N, K, pow2):
     x, w = _case(M * 7 + N, M, N, K, pow2)
     _check_linear(bi, x, w, pow2)
+
+
+@pytest.mark.parametrize("M,N,K", PREFILL_TMA)
+def test_prefill_kernels_agree(bi, M, N, K):
+    """The TMA-fed prefill kernel (f16 copies in the workspace) and the kernel
+    that converts the codes in its tile loop (a workspace without room for
+    the copies) give the same bits."""
+    x, w = _case(M * 5 + N, M, N, K, True)
+    q, s = quant_act(bi, x)
+    wq, sw = weights(bi, w, True)
+    full = bi.new_workspace(M, N, K)
+    f16 = sum((r * K * 2 + 255) // 256 * 256 for r in (M, N))
+    conv = torch.zeros(full.numel() - f16, dtype=torch.uint8, device="cuda")
+    assert torch.equal(linear(bi, q, s, wq, sw, ws=full), linear(bi, q, s, wq, sw, ws=conv))
 
 
 def test_linear_near_int32_bound(bi):
@@ -102,8 +120,12 @@ def test_prefill_split_tiles_leave_workspace_zeroed(bi):
     assert all(torch.equal(y, y_small) for y in ys)
     small = bi.new_workspace(16, N, K).numel()
     slots = 96 * 256 * 128 * 4
-    assert int(ws[:small].count_nonzero()) == 0 and int(ws[small + slots:].count_nonzero()) == 0
+    counters = small + slots + 768          # after them: the f16 operand copies (scratch)
+    assert int(ws[:small].count_nonzero()) == 0 and int(ws[small + slots:counters].count_nonzero()) == 0
     assert bi.bi_workspace_status(ws) == bi.BI_OK
+    # without room for the f16 copies the converting kernel runs, with the split
+    y_conv = linear(bi, q, s, wq, sw, ws=torch.zeros(counters, dtype=torch.uint8, device="cuda"))
+    assert torch.equal(y_conv, y_small)
 
 
 def test_pdl_flag_and_graph_capture_same_bits(bi):
