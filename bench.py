@@ -490,9 +490,11 @@ def prefill_measure(bi, torch, st, stream, peaks, Ms=(512, 2048)):
         tops = 2.0 * Mp * N * K / (ms * 1e-3) / 1e12
         out[str(Mp)] = {"ms": round(ms, 4), "tops": round(tops, 1),
                         "frac_of_bf16_peak": round(tops / float(peaks["bf16_tflops"]), 4)}
-    out["note"] = ("y = W8A8(x) with K=4096, N=12288 (int8 x int8 -> exact int32: int8 converted to f16 in "
-                   "shared memory, tcgen05.mma kind::f16 into fp32 TMEM chunks of 1024 K, int32 totals); "
-                   "peak = measured cuBLAS dense bf16, since sm_103a's tcgen05 has no int8 kind")
+    out["note"] = ("y = W8A8(x) with K=4096, N=12288 through bi_linear_w8a8 (int8 x int8 -> exact int32: above "
+                   "256 tokens a pass writes exact f16 copies of q and w into the workspace, then a persistent "
+                   "TMA-fed tcgen05.mma kind::f16 kernel accumulates fp32 TMEM chunks of 1024 K into int32 "
+                   "totals; the time includes the copy pass); peak = measured cuBLAS dense bf16, since "
+                   "sm_103a's tcgen05 has no int8 kind")
     return out
 
 
