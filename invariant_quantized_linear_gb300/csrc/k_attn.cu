@@ -683,23 +683,6 @@ __global__ void __launch_bounds__(kSmallThreads, 1) attn_chunk_small_kernel(Attn
 constexpr int kClusterCtas = 4;
 constexpr int kClusterThreads = 160;
 
-__device__ __forceinline__ uint32_t cluster_map(uint32_t local_smem, uint32_t rank)
-{
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_smem), "r"(rank));
-    return r;
-}
-
-__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v)
-{
-    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
-}
-
-__device__ __forceinline__ void cluster_sync_all()
-{
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
 template <int R>
 struct ClusterSmem {
     static constexpr int kD = 128;

@@ -240,6 +240,29 @@ __device__ __forceinline__ void pdl_launch_dependents()
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// ------------------------------------------------------------------ clusters
+
+// Address in the shared memory of CTA `rank` of the cluster that corresponds
+// to this CTA's shared address `local_smem`.
+__device__ __forceinline__ uint32_t cluster_map(uint32_t local_smem, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_smem), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v)
+{
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+// Every thread of every CTA of the cluster arrives (release) and waits
+// (acquire): the cluster's shared-memory writes before it are visible after.
+__device__ __forceinline__ void cluster_sync_all()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ misc
 
 // Swizzled byte offset of 16-byte chunk `chunk` (0..7) of row `row` inside a
