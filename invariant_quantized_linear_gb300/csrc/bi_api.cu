@@ -212,8 +212,6 @@ bi_status bi_linear_w8a8(const int8_t *q, const float *s_a, int M, int K, const 
         if (st != BI_OK) return st;
         st = bi::host::encode_f16_2d(&a.map_b, a.wf, N, K, 64, 256);
         if (st != BI_OK) return st;
-        st = bi::host::encode_f16_2d(&a.map_bs, a.wf, N, K, 64, 32);
-        if (st != BI_OK) return st;
         a.s_a = s_a;
         a.s_w = s_w;
         a.y = y;

@@ -27,13 +27,15 @@
 //              bf16_rne((float(acc) * s_a) * s_w).
 // The work of a CTA is a list of items: whole tiles (b, b + G, ...; tiles are
 // numbered token tile fastest, so the CTAs running together share weight
-// tiles in L2), then, when the last wave would be at most half full, one
-// slice of its tiles: the tile's 256 weight rows cut into slices of `tail_w`
-// rows (a multiple of 32), each run over the whole K by its own CTA with an
-// MMA of N = its width.  A slice needs no partial sums from other CTAs: on
-// this GPU, split-K partials exchanged through global memory made the
-// kernel's completion markedly slower (its written bytes are flushed at the
-// end).
+// tiles in L2), then, when the last wave would be at most half full, one K
+// half of one of its tiles.  The kernel is then launched in clusters of two
+// CTAs (as many pairs as fit at once), the two halves of a tile run on the
+// two CTAs of a pair, and their int32 sums meet in distributed shared memory:
+// each CTA owns every other group of 8 columns, receives its partner's sums of
+// those groups, adds them to its own and applies the epilogue.  Integer sums
+// are exact in any order, so the bits do not depend on the split.  (Partial
+// sums exchanged through global memory instead made the kernel's completion
+// markedly slower on this GPU.)
 // Every wait is bounded: on a timeout the kernel writes DEV_TIMEOUT to the
 // workspace status word and every role returns.
 #include "kernels.cuh"
@@ -72,20 +74,19 @@ struct Params {
     int vec_y;           // y rows allow 16-byte stores
     int tiles_m;         // token tiles (tile t: token tile t % tiles_m, weight tile t / tiles_m)
     int whole;           // tiles 0 .. whole - 1 run whole
-    int tail_w;          // later tiles run as slices of tail_w weight rows (multiple of 32)
-    int slices;          // ceil(256 / tail_w)
-    int tail_items;      // (tiles - whole) * slices: one per CTA 0 .. tail_items - 1
+    int tail_items;      // 2 * (tiles - whole): K halves, one per CTA 0 .. tail_items - 1 (clusters of 2)
     Workspace ws;
 };
 
-// One item of a CTA's list: a tile and the slice of its 256 weight rows.
+// One item of a CTA's list: a tile and its range of K steps.
 struct Item {
     int tile;
-    int c0, cw;          // weight rows c0 .. c0 + cw - 1 of the tile (cw a multiple of 32)
+    int kb, nsteps;
 };
 
 // Items of CTA b out of G: whole tiles b, b + G, ... below p.whole, then at
-// most one slice of a later tile (slice b of the (tiles - whole) * slices).
+// most one K half of a later tile (tile whole + b / 2, half b % 2 = the CTA's
+// rank in its cluster).
 __device__ __forceinline__ int item_count(const Params &p, int b, int G)
 {
     const int n_whole = b < p.whole ? (p.whole - 1 - b) / G + 1 : 0;
@@ -98,12 +99,12 @@ __device__ __forceinline__ Item item_at(const Params &p, int b, int G, int i)
     const int n_whole = b < p.whole ? (p.whole - 1 - b) / G + 1 : 0;
     if (i < n_whole) {
         it.tile = b + i * G;
-        it.c0 = 0;
-        it.cw = kTileN;
+        it.kb = 0;
+        it.nsteps = p.kt;
     } else {
-        it.tile = p.whole + b / p.slices;
-        it.c0 = (b % p.slices) * p.tail_w;
-        it.cw = min(p.tail_w, kTileN - it.c0);
+        it.tile = p.whole + (b >> 1);
+        it.kb = (b & 1) ? p.kt / 2 : 0;
+        it.nsteps = (b & 1) ? p.kt - p.kt / 2 : p.kt / 2;
     }
     return it;
 }
@@ -204,8 +205,7 @@ __device__ __forceinline__ void store_y8(uint16_t *yr, int n, int N, bool vec, f
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    prefill_tma_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-                       const __grid_constant__ CUtensorMap map_bs, Params p)
+    prefill_tma_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b, Params p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -247,12 +247,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     };
 
+    // a CTA with a K half (clusters of two): both CTAs of the pair meet in two
+    // cluster barriers after their roles, every thread of each (see below)
+    const bool pair = b < p.tail_items;
+
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
             prefetch_tensormap(&map_a);
             prefetch_tensormap(&map_b);
-            if (p.tail_items > 0) prefetch_tensormap(&map_bs);
             const uint64_t pol_a = policy_evict_last();    // token tile: reused by every weight tile
             const uint64_t pol_b = policy_evict_first();   // weight tile: read by the CTAs running together
             pdl_wait();   // the f16 copies come from the preceding expand pass
@@ -261,8 +264,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; ok && i < nitems; ++i) {
                 const Item it = item_at(p, b, G, i);
                 const int m0 = (it.tile % p.tiles_m) * kTileM;
-                const int n0 = (it.tile / p.tiles_m) * kTileN + it.c0;
-                for (int st = 0; st < p.kt; ++st, ++j) {
+                const int n0 = (it.tile / p.tiles_m) * kTileN;
+                for (int st = 0; st < it.nsteps; ++st, ++j) {
                     const int s = static_cast<int>(j % kStages);
                     if (j >= kStages && !mbar_wait_bounded(&empty[s], static_cast<uint32_t>((j / kStages) - 1) & 1u,
                                                            abort_flag)) {
@@ -271,15 +274,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     uint8_t *sa = smem + s * kStageBytes;
-                    mbar_arrive_expect_tx(&full[s], kStageA + it.cw * 128);
-                    const int k = st * kStepK;
+                    mbar_arrive_expect_tx(&full[s], kStageBytes);
+                    const int k = (it.kb + st) * kStepK;
                     tma_load_2d(sa, &map_a, &full[s], k, m0, pol_a);
-                    if (it.cw == kTileN) {
-                        tma_load_2d(sa + kStageA, &map_b, &full[s], k, n0, pol_b);
-                    } else {
-                        for (int r = 0; r < it.cw; r += 32)   // a slice: boxes of 32 weight rows
-                            tma_load_2d(sa + kStageA + r * 128, &map_bs, &full[s], k, n0 + r, pol_b);
-                    }
+                    tma_load_2d(sa + kStageA, &map_b, &full[s], k, n0, pol_b);
                 }
             }
             // let every issued copy land before the CTA can exit
@@ -287,14 +285,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (long long jj = j > kStages ? j - kStages : 0; jj < j; ++jj)
                 mbar_wait_bounded(&full[jj % kStages], static_cast<uint32_t>(jj / kStages) & 1u, &never);
         }
+        __syncwarp();
+        if (pair) {
+            cluster_sync_all();
+            cluster_sync_all();
+        }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issue
         long long j = 0, c = 0;
         bool ok = true;
         for (int i = 0; ok && i < nitems; ++i) {
             const Item it = item_at(p, b, G, i);
-            const uint32_t idesc = tc::idesc_f16_f32(kTileM, it.cw);
-            const int nch = (p.kt + kChunkSteps - 1) / kChunkSteps;
+            const uint32_t idesc = tc::idesc_f16_f32(kTileM, kTileN);
+            const int nch = (it.nsteps + kChunkSteps - 1) / kChunkSteps;
             for (int ch = 0; ok && ch < nch; ++ch, ++c) {
                 const int acc = static_cast<int>(c & 1);
                 if (c >= 2) {
@@ -304,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!ok) break;
                     tc::fence_after();
                 }
-                const int s0 = ch * kChunkSteps, s1 = min(p.kt, s0 + kChunkSteps);
+                const int s0 = ch * kChunkSteps, s1 = min(it.nsteps, s0 + kChunkSteps);
                 for (int st = s0; st < s1; ++st, ++j) {
                     const int s = static_cast<int>(j % kStages);
                     ok = __all_sync(0xffffffffu,
@@ -333,24 +336,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         volatile int never = 0;
         mbar_wait_bounded(drain, 0, &never);
+        __syncwarp();
+        if (pair) {
+            cluster_sync_all();
+            cluster_sync_all();
+        }
     } else {
         // ------------------------------------------------ chunk moves and epilogue
-        // thread: token row `row` of the tile, the item's weight rows
-        // c0 + half * cw / 2 .. + cw / 2 - 1 (at most 128: kCols)
+        // one token row and the column half `half` (128 columns) per thread
         const int qd = warp & 3;
         const int half = (warp - kEpiWarp0) >> 2;
         const int row = 32 * qd + lane;
-        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * qd) << 16);
-        const int nch = (p.kt + kChunkSteps - 1) / kChunkSteps;
-        long long c = 0;
         int32_t tot[kCols];
+        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * qd) << 16) + half * kCols;
+        long long c = 0;
         pdl_wait();   // scales and outputs follow the kernels before
         for (int i = 0; i < nitems; ++i) {
             const Item it = item_at(p, b, G, i);
             const int m0 = (it.tile % p.tiles_m) * kTileM;
-            const int hw = it.cw >> 1;                    // columns per half: a multiple of 16
-            const int col = half * hw;                    // first accumulator column of this thread
-            const int n0 = (it.tile / p.tiles_m) * kTileN + it.c0 + col;
+            const int n0 = (it.tile / p.tiles_m) * kTileN + half * kCols;
+            const int nch = (it.nsteps + kChunkSteps - 1) / kChunkSteps;
             bool ok = true;
             for (int ch = 0; ch < nch; ++ch, ++c) {
                 const int acc = static_cast<int>(c & 1);
@@ -364,15 +369,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc::fence_after();
 #pragma unroll
                 for (int g = 0; g < kCols / 16; ++g) {
-                    if (16 * g < hw) {
-                        uint32_t d[16];
-                        tc::ld16(lane_addr + acc * kTileN + col + 16 * g, d);
-                        tc::wait_ld();
+                    uint32_t d[16];
+                    tc::ld16(lane_addr + acc * kTileN + 16 * g, d);
+                    tc::wait_ld();
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const int32_t v = f2i_exact(__uint_as_float(d[e]));
-                            tot[16 * g + e] = ch > 0 ? tot[16 * g + e] + v : v;
-                        }
+                    for (int e = 0; e < 16; ++e) {
+                        const int32_t v = f2i_exact(__uint_as_float(d[e]));
+                        tot[16 * g + e] = ch > 0 ? tot[16 * g + e] + v : v;
                     }
                 }
                 tc::fence_before();
@@ -380,15 +383,59 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) mbar_arrive(&acc_empty[acc]);
             }
             if (!ok) break;
+            if (it.nsteps < p.kt) break;   // a K half: finished below, with the partner's sums
             const int tok = m0 + row;
             if (tok < p.M) {
                 const float sa = p.s_a[tok];
                 uint16_t *yr = p.y + static_cast<size_t>(tok) * p.N;
 #pragma unroll
                 for (int g = 0; g < kCols / 8; ++g)
-                    if (8 * g < hw) store_y8(yr, n0 + 8 * g, p.N, p.vec_y != 0, sa, p.s_w, tot + 8 * g);
+                    store_y8(yr, n0 + 8 * g, p.N, p.vec_y != 0, sa, p.s_w, tot + 8 * g);
             }
         }
+        if (pair) {
+        // The two K halves of a tile meet in distributed shared memory (both
+        // CTAs of the pair take this branch).  Column group g (8 columns)
+        // belongs to rank g % 2.  The ring is free once both CTAs have passed
+        // the first barrier (their copies landed, their MMAs drained); each
+        // then writes the groups it does not own into its partner's ring, and
+        // after the second barrier each adds them to its own and stores.
+        const int r = b & 1;
+        const uint32_t recv = smem_u32(smem);              // [16 groups][128 rows][8] int32
+        __syncwarp();
+        cluster_sync_all();
+        {
+#pragma unroll
+            for (int j = 0; j < kCols / 8; ++j) {
+                const int g = half * (kCols / 8) + j;
+                if ((g & 1) == r) continue;
+                const uint32_t dst = cluster_map(recv + static_cast<uint32_t>(((g >> 1) * kTileM + row) * 32), r ^ 1);
+                st_cluster_v4(dst, tot[8 * j], tot[8 * j + 1], tot[8 * j + 2], tot[8 * j + 3]);
+                st_cluster_v4(dst + 16, tot[8 * j + 4], tot[8 * j + 5], tot[8 * j + 6], tot[8 * j + 7]);
+            }
+        }
+        cluster_sync_all();
+        if (!*abort_flag) {
+            const Item it = item_at(p, b, G, nitems - 1);
+            const int tok = (it.tile % p.tiles_m) * kTileM + row;
+            const int n0 = (it.tile / p.tiles_m) * kTileN + half * kCols;
+            if (tok < p.M) {
+                const float sa = p.s_a[tok];
+                uint16_t *yr = p.y + static_cast<size_t>(tok) * p.N;
+#pragma unroll
+                for (int j = 0; j < kCols / 8; ++j) {
+                    const int g = half * (kCols / 8) + j;
+                    if ((g & 1) != r) continue;
+                    const int4 *src = reinterpret_cast<const int4 *>(smem + ((g >> 1) * kTileM + row) * 32);
+                    const int4 x0 = src[0], x1 = src[1];
+                    int32_t v[8] = {tot[8 * j] + x0.x,     tot[8 * j + 1] + x0.y, tot[8 * j + 2] + x0.z,
+                                    tot[8 * j + 3] + x0.w, tot[8 * j + 4] + x1.x, tot[8 * j + 5] + x1.y,
+                                    tot[8 * j + 6] + x1.z, tot[8 * j + 7] + x1.w};
+                    store_y8(yr, n0 + 8 * j, p.N, p.vec_y != 0, sa, p.s_w, v);
+                }
+            }
+        }
+    }
     }
     __syncwarp();
     tc::fence_before();
@@ -458,33 +505,39 @@ cudaError_t launch_prefill_tma(const PrefillTmaArgs &a, cudaStream_t stream)
     p.tiles_m = (a.M + kTileM - 1) / kTileM;
     const int tiles = p.tiles_m * ((a.N + kTileN - 1) / kTileN);
     p.whole = tiles;
-    p.tail_w = kTileN;
-    p.slices = 1;
     p.tail_items = 0;
-    // One CTA per SM.  Tiles that fill whole waves run whole; when the last
-    // wave would be at most half full, its tiles run as slices of the
-    // narrowest width (a multiple of 32 rows) whose slices all fit in it.
-    int grid = tiles < sms ? tiles : sms;
-    const int rem = tiles % sms;
-    if (rem > 0 && rem <= sms / 2) {
-        int w = 32;
-        while (w < kTileN && rem * ((kTileN + w - 1) / w) > sms) w += 32;
-        if (w < kTileN) {
-            p.whole = tiles - rem;
-            p.tail_w = w;
-            p.slices = (kTileN + w - 1) / w;
-            p.tail_items = rem * p.slices;
-            grid = p.whole > 0 ? sms : p.tail_items;
-        }
-    }
+    // One CTA per SM, all tiles whole; or, when the last wave would be at
+    // most half full, clusters of two CTAs (as many pairs as fit on the GPU at
+    // once) with the last wave's tiles split into K halves, one per CTA.
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = stream;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;   // a programmatic dependent of the expand pass (its TMA waits for it)
-    return cudaLaunchKernelEx(&cfg, prefill_tma_kernel, a.map_a, a.map_b, a.map_bs, p);
+    cudaLaunchAttribute lattr[2];
+    lattr[0] = attr[0];   // a programmatic dependent of the expand pass (its TMA waits for it)
+    lattr[1].id = cudaLaunchAttributeClusterDimension;
+    lattr[1].val.clusterDim.x = 2;
+    lattr[1].val.clusterDim.y = 1;
+    lattr[1].val.clusterDim.z = 1;
+    cfg.attrs = lattr;
+    int grid = tiles < sms ? tiles : sms;
+    if (tiles % sms != 0 && p.kt >= 16) {
+        cfg.numAttrs = 2;
+        cfg.gridDim = dim3(static_cast<unsigned>(sms));
+        int pairs = 0;
+        const cudaError_t e = cudaOccupancyMaxActiveClusters(&pairs, prefill_tma_kernel, &cfg);
+        if (e != cudaSuccess) return e;
+        const int g2 = 2 * pairs;
+        const int rem = g2 > 0 ? tiles % g2 : 0;
+        if (g2 > 0 && rem > 0 && 2 * rem <= g2) {
+            p.whole = tiles - rem;
+            p.tail_items = 2 * rem;
+            grid = p.whole > 0 ? g2 : p.tail_items;
+        }
+    }
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.numAttrs = p.tail_items > 0 ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, prefill_tma_kernel, a.map_a, a.map_b, p);
 }
 
 }  // namespace bi

@@ -125,7 +125,6 @@ struct PrefillTmaArgs {
     uint16_t *wf;              // [N, K] f16 copy (workspace)
     CUtensorMap map_a;         // qf: box 64 x 128, 128-byte swizzle
     CUtensorMap map_b;         // wf: box 64 x 256, 128-byte swizzle
-    CUtensorMap map_bs;        // wf: box 64 x 32 (slices of the last wave's tiles)
     const float *s_a;
     const float *s_w;
     uint16_t *y;

@@ -256,6 +256,12 @@ __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v)
     asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
+{
+    asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
 // Every thread of every CTA of the cluster arrives (release) and waits
 // (acquire): the cluster's shared-memory writes before it are visible after.
 __device__ __forceinline__ void cluster_sync_all()
