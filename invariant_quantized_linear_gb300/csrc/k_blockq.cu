@@ -91,34 +91,38 @@ __global__ void quantize_act_blocks_kernel(const uint16_t *__restrict__ x, int64
     if (lane == 0) d_a[static_cast<long long>(m) * nb + b] = s;
 }
 
-// 32 codes of one 32-block as unsigned bytes u = c + 32 in [0, 63], four per
-// word in element order.  Low nibbles: each ql word holds elements 8t .. 8t+7
-// (even ones in the low nibbles); masking gives the even and the odd
-// elements, and two byte permutes interleave them.  High bits: each qh word
-// holds elements 16s .. 16s+15 as 2-bit fields; four masked shifts put field j
-// of every byte at bits 4-5, and byte permutes gather them in element order.
-__device__ __forceinline__ void unpack32u(uint4 l, uint2 h, uint32_t (&u)[8])
+// 32 codes of one 32-block as unsigned bytes u = c + 32 in [0, 63], in the
+// order the stored bits give them cheaply: word 4q + j holds elements
+// 16q + j, 16q + 4 + j, 16q + 8 + j, 16q + 12 + j (q = 0, 1; j = 0 .. 3).
+// High bits: field j of every byte of qh word q, masked and moved to bits
+// 4-5.  Low nibbles: of the ql words 2q and 2q + 1, bytes 0 and 2 hold those
+// elements for j = 0, 1 (low, high nibble) and bytes 1 and 3 for j = 2, 3; one
+// byte permute gathers each pair.  The activations are stored in the same
+// order (act_natural_order), so the integer dot products are unchanged.
+__device__ __forceinline__ void unpack32n(uint4 l, uint2 h, uint32_t (&u)[8])
 {
     const uint32_t lw[4] = {l.x, l.y, l.z, l.w};
-#pragma unroll
-    for (int t = 0; t < 4; ++t) {
-        const uint32_t lo = lw[t] & 0x0F0F0F0Fu, hi = (lw[t] >> 4) & 0x0F0F0F0Fu;
-        u[2 * t] = __byte_perm(lo, hi, 0x5140);
-        u[2 * t + 1] = __byte_perm(lo, hi, 0x7362);
-    }
     const uint32_t hw[2] = {h.x, h.y};
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
         const uint32_t w = hw[q];
-        const uint32_t t0 = (w << 4) & 0x30303030u, t1 = (w << 2) & 0x30303030u;
-        const uint32_t t2 = w & 0x30303030u, t3 = (w >> 2) & 0x30303030u;
-        const uint32_t a01 = __byte_perm(t0, t1, 0x5140), a23 = __byte_perm(t2, t3, 0x5140);
-        const uint32_t b01 = __byte_perm(t0, t1, 0x7362), b23 = __byte_perm(t2, t3, 0x7362);
-        u[4 * q + 0] |= __byte_perm(a01, a23, 0x5410);
-        u[4 * q + 1] |= __byte_perm(a01, a23, 0x7632);
-        u[4 * q + 2] |= __byte_perm(b01, b23, 0x5410);
-        u[4 * q + 3] |= __byte_perm(b01, b23, 0x7632);
+        const uint32_t x0 = __byte_perm(lw[2 * q], lw[2 * q + 1], 0x6420);   // bytes 0, 2 of each
+        const uint32_t x1 = __byte_perm(lw[2 * q], lw[2 * q + 1], 0x7531);   // bytes 1, 3 of each
+        u[4 * q + 0] = (x0 & 0x0F0F0F0Fu) | ((w << 4) & 0x30303030u);
+        u[4 * q + 1] = ((x0 >> 4) & 0x0F0F0F0Fu) | ((w << 2) & 0x30303030u);
+        u[4 * q + 2] = (x1 & 0x0F0F0F0Fu) | (w & 0x30303030u);
+        u[4 * q + 3] = ((x1 >> 4) & 0x0F0F0F0Fu) | ((w >> 2) & 0x30303030u);
     }
+}
+
+// 16 activation bytes (elements 4i + k in byte k of word i) in the order of
+// unpack32n: word j = elements j, 4 + j, 8 + j, 12 + j (a 4 x 4 byte transpose).
+__device__ __forceinline__ uint4 act_natural_order(uint4 a)
+{
+    const uint32_t t01l = __byte_perm(a.x, a.y, 0x5140), t23l = __byte_perm(a.z, a.w, 0x5140);
+    const uint32_t t01h = __byte_perm(a.x, a.y, 0x7362), t23h = __byte_perm(a.z, a.w, 0x7362);
+    return make_uint4(__byte_perm(t01l, t23l, 0x5410), __byte_perm(t01l, t23l, 0x7632),
+                      __byte_perm(t01h, t23h, 0x5410), __byte_perm(t01h, t23h, 0x7632));
 }
 
 // sum over 4 byte pairs of (unsigned a byte) * (signed b byte), plus c
@@ -170,10 +174,11 @@ __host__ __device__ constexpr size_t q6_stage_bytes(int M, int K) { return stati
 // current one is computed), and each activation block is loaded once for the
 // warp's R rows.  MT and R change the work per thread, not the adds.
 // STAGED: the CTA first copies the activation codes and scales into shared
-// memory and forms each block's two sub-block sums once (instead of every
-// warp loading them from L1 and summing them per block); the block's two
-// 16-byte halves are stored swapped when bit 2 of its index is set, so that
-// 8 lanes reading 8 consecutive blocks hit distinct banks.
+// memory, forms each block's two sub-block sums and puts its codes in the
+// order of unpack32n once (instead of every warp loading them from L1 and
+// doing so per block); the block's two 16-byte halves are stored swapped when
+// bit 2 of its index is set, so that 8 lanes reading 8 consecutive blocks hit
+// distinct banks.
 template <int MT, int R, bool STAGED>
 __device__ __forceinline__ void linear_q6_body(const int8_t *__restrict__ qa, const float *__restrict__ d_a, int M,
                                                int K, const uint8_t *__restrict__ ql, const uint8_t *__restrict__ qh,
@@ -218,6 +223,8 @@ __device__ __forceinline__ void linear_q6_body(const int8_t *__restrict__ qa, co
             s1 = __dp4a(0x01010101, static_cast<int>(h1.z), s1);
             s1 = __dp4a(0x01010101, static_cast<int>(h1.w), s1);
             ssum[i] = make_int2(s0, s1);
+            *reinterpret_cast<uint4 *>(sact + static_cast<size_t>(i) * 32 + 16 * sw) = act_natural_order(h0);
+            *reinterpret_cast<uint4 *>(sact + static_cast<size_t>(i) * 32 + 16 * (sw ^ 1)) = act_natural_order(h1);
         }
         __syncthreads();
     }
@@ -239,7 +246,7 @@ __device__ __forceinline__ void linear_q6_body(const int8_t *__restrict__ qa, co
         }
         uint32_t u[R][8];                              // codes + 32, unsigned
 #pragma unroll
-        for (int r = 0; r < R; ++r) unpack32u(cur[r].l, cur[r].h, u[r]);
+        for (int r = 0; r < R; ++r) unpack32n(cur[r].l, cur[r].h, u[r]);
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
             if (m >= M) break;
@@ -267,6 +274,8 @@ __device__ __forceinline__ void linear_q6_body(const int8_t *__restrict__ qa, co
                 as1 = __dp4a(0x01010101, static_cast<int>(a1.y), as1);
                 as1 = __dp4a(0x01010101, static_cast<int>(a1.z), as1);
                 as1 = __dp4a(0x01010101, static_cast<int>(a1.w), as1);
+                a0 = act_natural_order(a0);
+                a1 = act_natural_order(a1);
             }
             const int a[8] = {static_cast<int>(a0.x), static_cast<int>(a0.y), static_cast<int>(a0.z),
                               static_cast<int>(a0.w), static_cast<int>(a1.x), static_cast<int>(a1.y),
