@@ -222,7 +222,7 @@ __device__ __forceinline__ void linear_q6_body(const int8_t *__restrict__ qa, co
             s1 = __dp4a(0x01010101, static_cast<int>(h1.y), s1);
             s1 = __dp4a(0x01010101, static_cast<int>(h1.z), s1);
             s1 = __dp4a(0x01010101, static_cast<int>(h1.w), s1);
-            ssum[i] = make_int2(s0, s1);
+            ssum[i] = make_int2(-32 * s0, -32 * s1);   // each sub-block's dp4a chain starts here
             *reinterpret_cast<uint4 *>(sact + static_cast<size_t>(i) * 32 + 16 * sw) = act_natural_order(h0);
             *reinterpret_cast<uint4 *>(sact + static_cast<size_t>(i) * 32 + 16 * (sw ^ 1)) = act_natural_order(h1);
         }
@@ -252,7 +252,8 @@ __device__ __forceinline__ void linear_q6_body(const int8_t *__restrict__ qa, co
             if (m >= M) break;
             uint4 a0, a1;
             float da;
-            int as0 = 0, as1 = 0;                      // sum(c a) = sum(u a) - 32 sum(a) per sub-block of 16
+            int as0 = 0, as1 = 0;                      // sum(c a) = sum(u a) - 32 sum(a) per sub-block of 16:
+                                                       // the dp4a chains start at -32 sum(a)
             if constexpr (STAGED) {
                 const size_t it = static_cast<size_t>(m) * nb + b;
                 const int sw = (b >> 2) & 1;
@@ -274,6 +275,8 @@ __device__ __forceinline__ void linear_q6_body(const int8_t *__restrict__ qa, co
                 as1 = __dp4a(0x01010101, static_cast<int>(a1.y), as1);
                 as1 = __dp4a(0x01010101, static_cast<int>(a1.z), as1);
                 as1 = __dp4a(0x01010101, static_cast<int>(a1.w), as1);
+                as0 *= -32;
+                as1 *= -32;
                 a0 = act_natural_order(a0);
                 a1 = act_natural_order(a1);
             }
@@ -282,13 +285,13 @@ __device__ __forceinline__ void linear_q6_body(const int8_t *__restrict__ qa, co
                               static_cast<int>(a1.z), static_cast<int>(a1.w)};
 #pragma unroll
             for (int r = 0; r < R; ++r) {
-                int s0 = 0, s1 = 0;
+                int s0 = as0, s1 = as1;
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     s0 = dp4a_us(u[r][k], a[k], s0);
                     s1 = dp4a_us(u[r][4 + k], a[4 + k], s1);
                 }
-                const int isum = cur[r].s.x * (s0 - 32 * as0) + cur[r].s.y * (s1 - 32 * as1);
+                const int isum = cur[r].s.x * s0 + cur[r].s.y * s1;
                 const float v = __fmul_rn(__fmul_rn(__int2float_rn(isum), da), cur[r].d);
                 p[m][r] = __fadd_rn(p[m][r], v);
             }
