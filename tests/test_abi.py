@@ -52,6 +52,19 @@ def test_workspace_sizes_positive(bi):
         assert bi.bi_lmhead_workspace_size(M, N, K) > 0
 
 
+def test_prefill_workspace_tiers(bi):
+    """The linear workspace has three sizes: the weight-streaming one (M <= 16),
+    plus the split-tile slots for 17 <= M <= 256 (independent of N and K), plus
+    room for the f16 copies of q and W (each rounded up to 256 bytes) above
+    256 tokens, where the TMA-fed prefill kernel reads them."""
+    small = bi.bi_linear_workspace_size(16, 12288, 4096)
+    mid = bi.bi_linear_workspace_size(17, 12288, 4096)
+    assert mid > small and bi.bi_linear_workspace_size(256, 5, 4096) == mid
+    f16 = lambda rows, K: (2 * rows * K + 255) // 256 * 256
+    for M, N, K in ((257, 4096, 272), (512, 12288, 4096), (2048, 12288, 4096), (1100, 2500, 1024)):
+        assert bi.bi_linear_workspace_size(M, N, K) == mid + f16(M, K) + f16(N, K)
+
+
 FAKE = 0x10000  # 16-byte aligned, never dereferenced
 
 
