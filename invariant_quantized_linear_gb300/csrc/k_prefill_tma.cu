@@ -117,6 +117,15 @@ __device__ __forceinline__ Item item_at(const Params &p, int b, int G, int i)
 constexpr int kExpandThreads = 256;
 constexpr int kExpandAhead = 4;
 
+// 16-byte store with an L2 evict-last policy: the copies are read by the
+// GEMM right after, so they should stay in L2.
+__device__ __forceinline__ void st_keep_l2(void *p, uint4 v, uint64_t pol)
+{
+    asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w), "l"(pol)
+                 : "memory");
+}
+
 __device__ __forceinline__ uint4 i8x8_to_f16x8(uint2 v)
 {
     uint4 r;
@@ -132,6 +141,7 @@ __global__ void __launch_bounds__(kExpandThreads) expand_f16_kernel(const int8_t
 {
     if (pdl) pdl_wait();
     const int lane = threadIdx.x & 31;
+    const uint64_t keep = policy_evict_last();
     const long long total = nq + nw;   // 512-code blocks: of q, then of w
     const long long nwarps = static_cast<long long>(gridDim.x) * (kExpandThreads / 32);
     long long blk = static_cast<long long>(blockIdx.x) * (kExpandThreads / 32) + (threadIdx.x >> 5);
@@ -151,8 +161,8 @@ __global__ void __launch_bounds__(kExpandThreads) expand_f16_kernel(const int8_t
             const long long c = blk + u * nwarps;
             if (c >= total) break;
             uint16_t *dst = (c < nq ? qf + 512 * c : wf + 512 * (c - nq)) + 8 * lane;
-            *reinterpret_cast<uint4 *>(dst) = i8x8_to_f16x8(v[u][0]);
-            *reinterpret_cast<uint4 *>(dst + 256) = i8x8_to_f16x8(v[u][1]);
+            st_keep_l2(dst, i8x8_to_f16x8(v[u][0]), keep);
+            st_keep_l2(dst + 256, i8x8_to_f16x8(v[u][1]), keep);
         }
     }
     pdl_launch_dependents();
