@@ -21,10 +21,10 @@
 //              ring;
 //   warp 1     allocates TMEM; lane 0 issues the MMAs and commits them;
 //   warps 2-9  (TMEM lane quarter = warp % 4, column half = (warp - 2) / 4)
-//              one token row and half of the item's weight columns (at
-//              most 128) per thread: add each chunk's sums into int32
-//              totals held in registers, then the epilogue
-//              bf16_rne((float(acc) * s_a) * s_w).
+//              one token row and 128 of the tile's 256 weight columns per
+//              thread: add each chunk's sums into int32 totals held in
+//              registers, then the epilogue bf16_rne((float(acc) * s_a) *
+//              s_w).
 // The work of a CTA is a list of items: whole tiles (b, b + G, ...; tiles are
 // numbered token tile fastest, so the CTAs running together share weight
 // tiles in L2), then, when the last wave would be at most half full, one K
@@ -36,8 +36,10 @@
 // are exact in any order, so the bits do not depend on the split.  (Partial
 // sums exchanged through global memory instead made the kernel's completion
 // markedly slower on this GPU.)
-// Every wait is bounded: on a timeout the kernel writes DEV_TIMEOUT to the
-// workspace status word and every role returns.
+// Every mbarrier wait is bounded: on a timeout the kernel writes DEV_TIMEOUT
+// to the workspace status word and every role returns.  The two cluster
+// barriers of a pair are then still reached by every thread of both CTAs (no
+// role returns early), so a timeout cannot leave a partner waiting.
 #include "kernels.cuh"
 #include "ptx.cuh"
 #include "tc.cuh"
